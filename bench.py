@@ -1,0 +1,446 @@
+"""Benchmark of the ZeRO-1 step for N simulated ranks on one GB300.
+
+    python bench.py [--gpus G] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...       # the CPU oracle as the reference arm
+
+Prints one JSON line.  `value` is whole-job throughput in GB/s of algorithmic
+bytes (N*P gradient reads + 24*P master/m/v read and write + N*P weight writes
+per step, the minimum the step must move), with every input resident in HBM.
+`e2e` is the same metric end to end through the public API with the step's
+gradients copied from pinned host memory and the global norm read back, every
+step.  `roofline` covers the dominant kernel, timed with CUDA events on its own
+launch stream inside the timed region.  `cpu_baseline` is the CPU oracle on a
+bounded window of the same workload.
+
+With G > 1 (torchrun, one process per GPU) every rank runs its own replica of
+the workload: the step has no cross-GPU exchange, so scaling is weak and
+`value` sums all ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import inputs as I  # noqa: E402
+
+METRIC = "ZeRO-1 step GB/s and % of GB300 HBM roofline; steps/s vs CPU oracle"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = I.GPT2_1P5B.name
+PROFILES = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = [os.path.join(ROOT, "gradient_reduction_zero_gb300", "csrc", f)
+                  for f in ("device.cuh", "reduce.cu", "adamw.cu", "internal.h")]
+
+
+# ------------------------------------------------------------------ bytes
+
+def step_bytes(w: I.Workload) -> int:
+    """Algorithmic bytes of one step (the minimum it must move)."""
+    eg, ew = w.grad_bytes(), w.weight_bytes()
+    if w.allreduce_only:
+        return 2 * w.N * w.P * eg
+    return w.N * w.P * eg + 24 * w.P + w.N * w.P * ew
+
+
+def kernel_bytes(name: str, w: I.Workload) -> int:
+    """Algorithmic bytes of one launch of each kernel."""
+    N, P, eg, ew = w.N, w.P, w.grad_bytes(), w.weight_bytes()
+    return {
+        "dpz_rs_avg_sumsq": N * P * eg + P * eg,
+        "dpz_rs_avg": N * P * eg + P * eg,
+        "dpz_adamw_bcast": P * eg + 24 * P + N * P * ew,
+        "dpz_adamw_owner": P * eg + 24 * P + P * ew,
+        "dpz_zero1_fused": N * P * eg + 24 * P + N * P * ew,
+        "dpz_zero1_fused_sumsq": N * P * eg + 24 * P + N * P * ew,
+        "dpz_allreduce_avg": 2 * N * P * eg,
+        "dpz_allgather": N * P * ew,
+        "dpz_norm_owned": P * eg,
+        "dpz_norm_finalize": 8 * N * ((P // N + 255) // 256),
+    }.get(name, 0)
+
+
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, w: I.Workload):
+    """DRAM bytes per launch from the committed ncu summary, scaled to this
+    workload by the units processed; None if absent or the kernels changed."""
+    path = os.path.join(PROFILES, "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    if t.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    k = t.get("kernels", {}).get(kernel)
+    if not k or k.get("N") != w.N:
+        return None
+    return int(k["dram_bytes_per_element"] * w.P)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t_lo: float, t_hi: float) -> dict | None:
+        """Summary of the samples taken between host times t_lo and t_hi."""
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, ln in self.lines:
+            if ts < t_lo or ts > t_hi:
+                continue
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ ranks
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_window_step(w: I.Workload, width: int, offset: int = 0):
+    """Inputs for one oracle step on a window of `width` elements of every
+    chunk (a mini-arena of N*width elements per rank), generated up front."""
+    g = I.window_arena_host(w, offset, width)
+    th = I.window_state_host(w, "master", offset, width)
+    m = I.window_state_host(w, "m", offset, width)
+    v = I.window_state_host(w, "v", offset, width)
+    wt = np.zeros((w.N, w.N * width), dtype=np.uint16 if w.wdtype == "bf16" else np.float32)
+    return g, th, m, v, wt
+
+
+def time_oracle(w: I.Workload, seconds: float) -> dict:
+    """The oracle as it stands, single-threaded, on windows of the workload
+    until about `seconds` of CPU time; throughput in the metric's unit."""
+    import oracle as O
+    width = min(w.C, 1 << 18)
+    cfg = O.cfg_from_workload(w)
+    mini = w.with_(P=w.N * width)
+    base = oracle_window_step(w, width, offset=(w.C - width) // 2)
+    done_bytes, elapsed, reps = 0, 0.0, 0
+    while elapsed < seconds or reps == 0:
+        args = [a.copy() for a in base]
+        t0 = time.perf_counter()
+        if w.allreduce_only:
+            O.ring_allreduce_avg(args[0])
+        else:
+            # the window's own norm stands in for the arena's: same work
+            O.zero1_step(*args, cfg)
+        elapsed += time.perf_counter() - t0
+        done_bytes += step_bytes(mini)
+        reps += 1
+    return {"value": done_bytes / elapsed / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} windows of {width} elements per chunk x {w.N} chunks x {w.N} ranks "
+                      f"of {w.name} ({elapsed:.1f} s single-threaded)"}
+
+
+def run_reference(args) -> None:
+    """The CPU oracle timed as the reference arm: rank 0 only, each step a
+    bounded window of the workload, the whole run kept to a few minutes."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    w = I.WORKLOADS[args.workload]
+    per_step = []
+    secs = min(args.ref_seconds, 150.0 / max(1, args.warmup + args.steps))
+    for i in range(args.warmup + args.steps):
+        r = time_oracle(w, secs)
+        if i >= args.warmup:
+            per_step.append(r)
+    vals = [r["value"] for r in per_step]
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_bytes(w) / (value * 1e9) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": per_step[-1]["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w: I.Workload) -> dict:
+    c = {"workload": w.name, "ranks_simulated": w.N, "P": w.P, "grad_dtype": w.gdtype,
+         "weight_dtype": w.wdtype, "state_dtype": "f32" if not w.allreduce_only else None,
+         "clip": w.clip, "step_t": w.step,
+         "l2": "inputs larger than L2 (resident arena %.1f GB vs 129 MB L2)" % (
+             (w.N * w.P * (w.grad_bytes() + w.weight_bytes()) + 12 * w.P) / 1e9),
+         "parallelism": f"{w.N} simulated ranks per GPU"}
+    return c
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def allocate(w: I.Workload, dev):
+    import torch
+    gd = torch.bfloat16 if w.gdtype == "bf16" else torch.float32
+    wd = torch.bfloat16 if w.wdtype == "bf16" else torch.float32
+    G = torch.empty(w.N * w.P, dtype=gd, device=dev)
+    I.fill_grads_device(w, G)
+    if w.allreduce_only:
+        return G, None, None, None, None
+    T = torch.empty(w.P, dtype=torch.float32, device=dev)
+    M = torch.empty_like(T)
+    V = torch.empty_like(T)
+    for which, t in (("master", T), ("m", M), ("v", V)):
+        I.fill_state_device(w, which, t)
+    W = torch.zeros(w.N * w.P, dtype=wd, device=dev)
+    return G, T, M, V, W
+
+
+def run_gpu(args) -> None:
+    import torch
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import gradient_reduction_zero_gb300.dpz as dpz
+
+    w = I.WORKLOADS[args.workload]
+    G, T, M, V, W = allocate(w, dev)
+    ws = dpz.workspace(w.P, w.N, dev)
+    nrm = torch.zeros(1, dtype=torch.float32, device=dev)
+    cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        if w.allreduce_only:
+            dpz.dp_allreduce_avg(G, w.N, stream)
+        else:
+            dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    # ---------------------------------------------------------------- timed
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    launches0 = dpz.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    dpz.profile_start(16 * args.steps + 16)
+    t_lo = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_hi = time.time()
+    barrier(world)
+    kstats = dpz.profile_stop()
+    launches = dpz.launch_count() - launches0
+    time.sleep(0.2)
+    clk = clocks.stop(t_lo, t_hi)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, world)
+
+    nbytes = step_bytes(w)
+    value = nbytes * world / (ms_max * 1e-3) / 1e9
+    pk = peaks()
+
+    # dominant kernel: largest share of the timed region
+    dom = max(kstats.items(), key=lambda kv: kv[1][1])
+    dname, (dn, dms) = dom
+    per_launch_ms = dms / dn
+    kb = kernel_bytes(dname, w)
+    achieved = kb / (per_launch_ms * 1e-3) / 1e9
+    shares = {k: {"launches": n, "ms_total": round(t, 4),
+                  "share": round(t / sum(x[1] for x in kstats.values()), 4)}
+              for k, (n, t) in kstats.items()}
+
+    # ---------------------------------------------------------------- e2e
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, G, step, nrm, stream, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_max, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": config_of(w),
+            "steps_per_s": round(1e3 / ms_max, 3),
+            "pct_of_hbm_roofline": {
+                "measured_copy_peak": round(100 * value / world / pk["hbm_gbs"], 2),
+                "spec_8tbs": round(100 * value / world / 8000.0, 2)},
+            "bytes_per_step": nbytes,
+            "roofline": {"bound": "hbm", "kernel": dname, "achieved": round(achieved, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / pk["hbm_gbs"], 4),
+                         "traffic": ncu_traffic(dname, w),
+                         "algorithmic_bytes_per_launch": kb,
+                         "ms_per_launch": round(per_launch_ms, 4),
+                         "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
+            "kernels": shares,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, G, step, nrm, stream, world):
+    """Same step through the public API with the gradients coming from pinned
+    host memory and the norm read back, every step."""
+    import torch
+    host = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
+    host.copy_(G)
+    torch.cuda.synchronize()
+
+    def one():
+        G.copy_(host, non_blocking=True)
+        step()
+        return nrm.item() if not w.allreduce_only else G[:1].item()
+
+    for _ in range(1):
+        one()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / args.e2e_steps
+    dt = max_over_ranks(dt, world)
+    d2h = 4 if not w.allreduce_only else G.element_size()
+    return {"value": round(step_bytes(w) * world / dt / 1e9, 2), "unit": UNIT,
+            "ms_per_step": round(dt * 1e3, 3),
+            "h2d_bytes_per_step": G.numel() * G.element_size(), "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["dpz", "reference"], default="dpz")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=4.0)
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,135 @@
+// Optimizer-side kernel: sharded AdamW on every rank's owned chunk, the cast
+// to the weight dtype, and the write of the new weights into the owner slab
+// (zero1_adamw_step) or into all N slabs (the fused all-gather).  The averaged
+// gradient is either loaded from the owner slab (after a reduce-scatter) or
+// computed in place by the ring fold (the single-kernel step without clip).
+#include "device.cuh"
+#include "internal.h"
+
+namespace dpz {
+
+template <int GDT, int WDT, bool FOLD, bool BCAST, bool SUMSQ>
+__global__ void __launch_bounds__(kBlock)
+k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
+        float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int N,
+        Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
+        double* __restrict__ partials)
+{
+    constexpr int GES = Group<GDT>::kBytes;
+    constexpr int WES = Group<WDT>::kBytes;
+    const int64_t gslab = P * GES;
+    const int64_t wslab = P * WES;
+    const int64_t groups = C / kGroup;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+
+    // clip scale from the global norm of the averaged gradient
+    float scale = 1.0f;
+    bool do_scale = false;
+    if (!FOLD && h.clip > 0.0f) {
+        const float nrm = hdr->norm;
+        if (nrm > h.clip) {
+            scale = __fdiv_rn(h.clip, nrm);
+            do_scale = true;
+        }
+    }
+
+    const int64_t segs = segments_per_chunk(C);
+    const int lane = threadIdx.x & 31;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
+    if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
+    for (int c = 0; c < N; ++c) {
+        for (int64_t wb = first; wb < groups; wb += stride) {
+            const int64_t gi = wb + lane;
+            float ss = 0.0f;
+            if (gi < groups) {
+                const int64_t e = c * C + gi * kGroup;  // element index (same in every slab)
+                float g[8];
+                if (FOLD) {
+                    ring_fold<GDT>(grads, gslab, e * GES, c, N, g);
+                    average8<GDT>(g, avg);
+                    if (SUMSQ) ss = sumsq8(g);
+                    if (store_avg) store_group<GDT>(grads + c * gslab + e * GES, g);
+                } else {
+                    load_group<GDT>(grads + c * gslab + e * GES, g);
+                }
+                float th[8], mm[8], vv[8];
+                load_group<0>(reinterpret_cast<const char*>(master + e), th);
+                load_group<0>(reinterpret_cast<const char*>(mom + e), mm);
+                load_group<0>(reinterpret_cast<const char*>(var + e), vv);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float gq = do_scale ? __fmul_rn(g[q], scale) : g[q];
+                    adamw_elem(th[q], mm[q], vv[q], gq, h);
+                }
+                store_group<0>(reinterpret_cast<char*>(master + e), th);
+                store_group<0>(reinterpret_cast<char*>(mom + e), mm);
+                store_group<0>(reinterpret_cast<char*>(var + e), vv);
+                const typename Group<WDT>::Raw w = Group<WDT>::pack(th);
+                if (BCAST) {
+                    for (int r = 0; r < N; ++r)
+                        Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
+                } else {
+                    Group<WDT>::store_raw(weights + c * wslab + e * WES, w);
+                }
+            }
+            if (SUMSQ) {
+                const double t = warp_sum((double)ss);
+                if (lane == 0) partials[c * segs + wb / 32] = t;
+            }
+        }
+    }
+}
+
+template <int GDT, int WDT, bool FOLD, bool BCAST, bool SUMSQ>
+static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
+                           void* grads, float* master, float* m, float* v, void* weights,
+                           void* ws, cudaStream_t s)
+{
+    auto fn = k_adamw<GDT, WDT, FOLD, BCAST, SUMSQ>;
+    const int grid = grid_for((const void*)fn, a.C / kGroup, 0);
+    set_last_kernel_name(FOLD ? (SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused")
+                              : (BCAST ? "dpz_adamw_bcast" : "dpz_adamw_owner"));
+    fn<<<grid, kBlock, 0, s>>>(static_cast<char*>(grads), master, m, v,
+                               static_cast<char*>(weights), a.P, a.C, a.N, avg, h,
+                               store_avg ? 1 : 0, static_cast<WsHeader*>(ws),
+                               SUMSQ ? ws_partials(ws) : nullptr);
+    return cudaGetLastError();
+}
+
+template <int GDT, int WDT>
+static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
+                            bool bcast, bool store_avg, void* grads, float* master, float* m,
+                            float* v, void* weights, void* ws, cudaStream_t s)
+{
+    if (src == AdamSrc::kFold) {
+        if (ws != nullptr)
+            return adamw_t<GDT, WDT, true, true, true>(a, avg, h, store_avg, grads, master, m, v,
+                                                      weights, ws, s);
+        return adamw_t<GDT, WDT, true, true, false>(a, avg, h, store_avg, grads, master, m, v,
+                                                   weights, ws, s);
+    }
+    if (bcast)
+        return adamw_t<GDT, WDT, false, true, false>(a, avg, h, false, grads, master, m, v,
+                                                    weights, ws, s);
+    return adamw_t<GDT, WDT, false, false, false>(a, avg, h, false, grads, master, m, v, weights,
+                                                 ws, s);
+}
+
+cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
+                         bool bcast, bool store_avg, void* grads, float* master, float* m,
+                         float* v, void* weights, void* ws, cudaStream_t s)
+{
+    if (a.gdt == 1 && a.wdt == 1)
+        return adamw_dt<1, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws,
+                              s);
+    if (a.gdt == 1 && a.wdt == 0)
+        return adamw_dt<1, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws,
+                              s);
+    if (a.gdt == 0 && a.wdt == 1)
+        return adamw_dt<0, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws,
+                              s);
+    return adamw_dt<0, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws,
+                          s);
+}
+
+}  // namespace dpz

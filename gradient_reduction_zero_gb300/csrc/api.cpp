@@ -1,0 +1,386 @@
+// The C-ABI of include/dpz.h: argument checks, status codes, the last-error
+// message, launch accounting and optional per-launch event timing.  Every
+// entry point validates all of its arguments before it launches anything.
+#include "dpz.h"
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using namespace dpz;
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<int64_t> g_launches{0};
+
+int fail(int code, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int ok()
+{
+    g_err.clear();
+    return DPZ_OK;
+}
+
+int elem_bytes(int dt) { return dt == DPZ_BF16 ? 2 : 4; }
+
+// ------------------------------------------------------------ validation
+
+int check_dims(int64_t P, int N)
+{
+    if (N < 1 || N > DPZ_MAX_RANKS)
+        return fail(DPZ_ERR_INVALID_ARG, "N = %d is outside 1..%d", N, DPZ_MAX_RANKS);
+    if (P <= 0) return fail(DPZ_ERR_INVALID_ARG, "P = %lld must be positive", (long long)P);
+    if (P > (int64_t(1) << 40))
+        return fail(DPZ_ERR_INVALID_ARG, "P = %lld exceeds 2^40", (long long)P);
+    if (P % N != 0)
+        return fail(DPZ_ERR_INVALID_ARG,
+                    "P = %lld is not divisible by N = %d: the arena cannot be sharded equally",
+                    (long long)P, N);
+    if ((P / N) % kGroup != 0)
+        return fail(DPZ_ERR_ALIGN,
+                    "chunk P/N = %lld is not a multiple of 8 elements (16-byte chunks); "
+                    "pad P to a multiple of 8*N",
+                    (long long)(P / N));
+    return DPZ_OK;
+}
+
+int check_dtype(int dt, const char* what)
+{
+    if (dt != DPZ_F32 && dt != DPZ_BF16)
+        return fail(DPZ_ERR_INVALID_ARG, "%s dtype %d is neither DPZ_F32 nor DPZ_BF16", what, dt);
+    return DPZ_OK;
+}
+
+int check_ptr(const void* p, const char* what)
+{
+    if (p == nullptr) return fail(DPZ_ERR_INVALID_ARG, "%s is NULL", what);
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+        return fail(DPZ_ERR_ALIGN, "%s is not 16-byte aligned", what);
+    return DPZ_OK;
+}
+
+struct Range {
+    const char* name;
+    uintptr_t lo, hi;
+};
+
+int check_disjoint(const std::vector<Range>& rs)
+{
+    for (size_t i = 0; i < rs.size(); ++i)
+        for (size_t j = i + 1; j < rs.size(); ++j)
+            if (rs[i].lo < rs[j].hi && rs[j].lo < rs[i].hi)
+                return fail(DPZ_ERR_INVALID_ARG, "buffers %s and %s overlap", rs[i].name,
+                            rs[j].name);
+    return DPZ_OK;
+}
+
+Range range(const char* name, const void* p, int64_t bytes)
+{
+    uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return {name, lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+int check_cfg(const dpz_adamw_cfg* cfg)
+{
+    if (cfg == nullptr) return fail(DPZ_ERR_INVALID_ARG, "cfg is NULL");
+    if (cfg->step < 1)
+        return fail(DPZ_ERR_INVALID_ARG, "step = %lld must be >= 1", (long long)cfg->step);
+    return DPZ_OK;
+}
+
+#define DPZ_TRY(x)                     \
+    do {                               \
+        int rc_ = (x);                 \
+        if (rc_ != DPZ_OK) return rc_; \
+    } while (0)
+
+Arena make_arena(int64_t P, int N, int gdt, int wdt)
+{
+    return Arena{P, P / N, N, gdt, wdt};
+}
+
+Avg make_avg(int N)
+{
+    Avg a;
+    a.fN = static_cast<float>(N);
+    a.pow2 = (N & (N - 1)) == 0;
+    a.invN = 1.0f / static_cast<float>(N);
+    return a;
+}
+
+AdamArgs make_adam(const dpz_adamw_cfg* cfg)
+{
+    AdamArgs h;
+    h.lr = cfg->lr;
+    h.b1 = cfg->beta1;
+    h.b2 = cfg->beta2;
+    h.omb1 = 1.0f - cfg->beta1;
+    h.omb2 = 1.0f - cfg->beta2;
+    h.bc1 = static_cast<float>(1.0 - std::pow(static_cast<double>(cfg->beta1),
+                                              static_cast<double>(cfg->step)));
+    h.bc2 = static_cast<float>(1.0 - std::pow(static_cast<double>(cfg->beta2),
+                                              static_cast<double>(cfg->step)));
+    h.eps = cfg->eps;
+    h.wd = cfg->weight_decay;
+    h.clip = cfg->clip_norm;
+    return h;
+}
+
+// ------------------------------------------------------------ profiling
+
+struct Profiler {
+    std::mutex mu;
+    bool on = false;
+    int cap = 0;
+    int used = 0;
+    std::vector<cudaEvent_t> ev;
+    std::vector<std::string> names;
+};
+Profiler g_prof;
+
+template <class F>
+int launch(cudaStream_t s, F&& f)
+{
+    int slot = -1;
+    {
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        if (g_prof.on && g_prof.used < g_prof.cap) slot = g_prof.used++;
+    }
+    if (slot >= 0) cudaEventRecord(g_prof.ev[2 * slot], s);
+    cudaError_t e = f();
+    const char* name = last_kernel_name();
+    if (slot >= 0) {
+        cudaEventRecord(g_prof.ev[2 * slot + 1], s);
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        g_prof.names[slot] = name;
+    }
+    if (e != cudaSuccess)
+        return fail(DPZ_ERR_CUDA, "launch of %s failed: %s", name, cudaGetErrorString(e));
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return DPZ_OK;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+// ====================================================================== ABI
+
+extern "C" {
+
+DPZ_API size_t dpz_workspace_bytes(int64_t P, int N)
+{
+    if (N < 1 || N > DPZ_MAX_RANKS || P <= 0 || P % N != 0) return 0;
+    return ws_bytes_for(P, N);
+}
+
+DPZ_API const char* dpz_last_error(void) { return g_err.c_str(); }
+
+DPZ_API const char* dpz_version(void) { return "dpz 0.1 (sm_103a)"; }
+
+DPZ_API int64_t dpz_launch_count(void) { return g_launches.load(); }
+
+DPZ_API int dp_reduce_scatter_avg(void* grads, int64_t P, int N, int gdtype, void* stream)
+{
+    DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_dtype(gdtype, "gradient"));
+    DPZ_TRY(check_ptr(grads, "grads"));
+    const Arena a = make_arena(P, N, gdtype, gdtype);
+    const Avg avg = make_avg(N);
+    DPZ_TRY(launch(as_stream(stream), [&] {
+        return launch_reduce(a, avg, grads, false, nullptr, as_stream(stream));
+    }));
+    return ok();
+}
+
+DPZ_API int dp_allreduce_avg(void* grads, int64_t P, int N, int gdtype, void* stream)
+{
+    DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_dtype(gdtype, "gradient"));
+    DPZ_TRY(check_ptr(grads, "grads"));
+    const Arena a = make_arena(P, N, gdtype, gdtype);
+    const Avg avg = make_avg(N);
+    DPZ_TRY(launch(as_stream(stream), [&] {
+        return launch_reduce(a, avg, grads, true, nullptr, as_stream(stream));
+    }));
+    return ok();
+}
+
+DPZ_API int dp_grad_global_norm(const void* grads, int64_t P, int N, int gdtype, void* ws,
+                                float* norm_out, void* stream)
+{
+    DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_dtype(gdtype, "gradient"));
+    DPZ_TRY(check_ptr(grads, "grads"));
+    DPZ_TRY(check_ptr(ws, "ws"));
+    std::vector<Range> rs = {range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
+                             range("ws", ws, (int64_t)dpz_workspace_bytes(P, N))};
+    if (norm_out) rs.push_back(range("norm_out", norm_out, 4));
+    DPZ_TRY(check_disjoint(rs));
+    const Arena a = make_arena(P, N, gdtype, gdtype);
+    cudaStream_t s = as_stream(stream);
+    DPZ_TRY(launch(s, [&] { return launch_norm_owned(a, grads, ws, s); }));
+    DPZ_TRY(launch(s, [&] { return launch_norm_finalize(a, ws, norm_out, s); }));
+    return ok();
+}
+
+static int check_step_buffers(const void* grads, const float* master, const float* m,
+                              const float* v, const void* weights, int64_t P, int N, int gdtype,
+                              int wdtype, const dpz_adamw_cfg* cfg, const void* ws, bool need_ws,
+                              const float* norm_out)
+{
+    DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_dtype(gdtype, "gradient"));
+    DPZ_TRY(check_dtype(wdtype, "weight"));
+    DPZ_TRY(check_cfg(cfg));
+    DPZ_TRY(check_ptr(grads, "grads"));
+    DPZ_TRY(check_ptr(master, "master"));
+    DPZ_TRY(check_ptr(m, "m"));
+    DPZ_TRY(check_ptr(v, "v"));
+    DPZ_TRY(check_ptr(weights, "weights"));
+    if (need_ws) DPZ_TRY(check_ptr(ws, "ws"));
+    std::vector<Range> rs = {range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
+                             range("master", master, P * 4), range("m", m, P * 4),
+                             range("v", v, P * 4),
+                             range("weights", weights, int64_t(N) * P * elem_bytes(wdtype))};
+    if (ws) rs.push_back(range("ws", ws, (int64_t)dpz_workspace_bytes(P, N)));
+    if (norm_out) rs.push_back(range("norm_out", norm_out, 4));
+    return check_disjoint(rs);
+}
+
+DPZ_API int zero1_adamw_step(const void* grads, float* master, float* m, float* v,
+                             void* weights, int64_t P, int N, int gdtype, int wdtype,
+                             const dpz_adamw_cfg* cfg, const void* ws, void* stream)
+{
+    const bool clip = cfg != nullptr && cfg->clip_norm > 0.0f;
+    DPZ_TRY(check_step_buffers(grads, master, m, v, weights, P, N, gdtype, wdtype, cfg, ws, clip,
+                               nullptr));
+    const Arena a = make_arena(P, N, gdtype, wdtype);
+    const Avg avg = make_avg(N);
+    const AdamArgs h = make_adam(cfg);
+    cudaStream_t s = as_stream(stream);
+    DPZ_TRY(launch(s, [&] {
+        return launch_adamw(a, avg, h, AdamSrc::kLoadOwner, false, false,
+                            const_cast<void*>(grads), master, m, v, weights,
+                            const_cast<void*>(ws), s);
+    }));
+    return ok();
+}
+
+DPZ_API int dp_allgather(void* weights, int64_t P, int N, int wdtype, void* stream)
+{
+    DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_dtype(wdtype, "weight"));
+    DPZ_TRY(check_ptr(weights, "weights"));
+    const Arena a = make_arena(P, N, wdtype, wdtype);
+    cudaStream_t s = as_stream(stream);
+    DPZ_TRY(launch(s, [&] { return launch_allgather(a, weights, s); }));
+    return ok();
+}
+
+DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v, void* weights,
+                          int64_t P, int N, int gdtype, int wdtype, const dpz_adamw_cfg* cfg,
+                          void* ws, float* norm_out, void* stream)
+{
+    const bool clip = cfg != nullptr && cfg->clip_norm > 0.0f;
+    DPZ_TRY(check_step_buffers(grads, master, m, v, weights, P, N, gdtype, wdtype, cfg, ws,
+                               clip || norm_out != nullptr, norm_out));
+    const Arena a = make_arena(P, N, gdtype, wdtype);
+    const Avg avg = make_avg(N);
+    const AdamArgs h = make_adam(cfg);
+    cudaStream_t s = as_stream(stream);
+    if (clip) {
+        // reduce-scatter + average + norm partials, then the norm, then AdamW +
+        // cast + all-gather reading the stored averages
+        DPZ_TRY(launch(s, [&] { return launch_reduce(a, avg, grads, false, ws, s); }));
+        DPZ_TRY(launch(s, [&] { return launch_norm_finalize(a, ws, norm_out, s); }));
+        DPZ_TRY(launch(s, [&] {
+            return launch_adamw(a, avg, h, AdamSrc::kLoadOwner, true, false, grads, master, m, v,
+                                weights, ws, s);
+        }));
+    } else {
+        void* sws = norm_out ? ws : nullptr;
+        DPZ_TRY(launch(s, [&] {
+            return launch_adamw(a, avg, h, AdamSrc::kFold, true, cfg->store_avg != 0, grads,
+                                master, m, v, weights, sws, s);
+        }));
+        if (norm_out)
+            DPZ_TRY(launch(s, [&] { return launch_norm_finalize(a, ws, norm_out, s); }));
+    }
+    return ok();
+}
+
+DPZ_API int dpz_profile_start(int max_launches)
+{
+    if (max_launches < 1 || max_launches > (1 << 20))
+        return fail(DPZ_ERR_INVALID_ARG, "max_launches = %d is outside 1..2^20", max_launches);
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    for (cudaEvent_t e : g_prof.ev) cudaEventDestroy(e);
+    g_prof.ev.assign(2 * static_cast<size_t>(max_launches), nullptr);
+    g_prof.names.assign(static_cast<size_t>(max_launches), std::string());
+    for (auto& e : g_prof.ev) {
+        cudaError_t rc = cudaEventCreate(&e);
+        if (rc != cudaSuccess) {
+            g_prof.on = false;
+            return fail(DPZ_ERR_CUDA, "cudaEventCreate failed: %s", cudaGetErrorString(rc));
+        }
+    }
+    g_prof.cap = max_launches;
+    g_prof.used = 0;
+    g_prof.on = true;
+    return ok();
+}
+
+DPZ_API int dpz_profile_stop(dpz_kernel_stat* stats, int max_stats, int* n_stats)
+{
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    g_prof.on = false;
+    std::vector<dpz_kernel_stat> out;
+    for (int i = 0; i < g_prof.used; ++i) {
+        cudaError_t rc = cudaEventSynchronize(g_prof.ev[2 * i + 1]);
+        if (rc != cudaSuccess)
+            return fail(DPZ_ERR_CUDA, "cudaEventSynchronize failed: %s", cudaGetErrorString(rc));
+        float ms = 0.0f;
+        rc = cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]);
+        if (rc != cudaSuccess)
+            return fail(DPZ_ERR_CUDA, "cudaEventElapsedTime failed: %s", cudaGetErrorString(rc));
+        const std::string& nm = g_prof.names[i];
+        dpz_kernel_stat* hit = nullptr;
+        for (auto& st : out)
+            if (nm == st.name) hit = &st;
+        if (!hit) {
+            dpz_kernel_stat st{};
+            std::snprintf(st.name, sizeof st.name, "%s", nm.c_str());
+            out.push_back(st);
+            hit = &out.back();
+        }
+        hit->launches += 1;
+        hit->total_ms += ms;
+    }
+    const int n = static_cast<int>(out.size());
+    if (n_stats) *n_stats = n;
+    if (stats)
+        for (int i = 0; i < n && i < max_stats; ++i) stats[i] = out[i];
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// Internal interface between the C-ABI layer (api.cpp) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define DPZ_HD __host__ __device__
+#else
+#define DPZ_HD
+#endif
+
+namespace dpz {
+
+constexpr int kGroup = 8;             // elements a thread handles at once
+constexpr int kBlock = 256;           // threads per block of the streaming kernels
+constexpr int kSegment = 32 * kGroup; // elements per norm partial (one warp-iteration)
+constexpr int kFinalBlocks = 256;     // most blocks of the norm finalisation
+constexpr int kFinalThreads = 512;
+constexpr size_t kWsHeaderBytes = 256;
+
+// Start of the workspace (device memory).  Then kFinalBlocks doubles of
+// first-stage sums, then one double per 256-element segment of every chunk.
+struct WsHeader {
+    double sumsq;      // global sum of squares of the averaged gradient
+    float norm;        // sqrt(sumsq) rounded to float
+    uint32_t nparts;   // segment partials the last norm used
+    uint32_t arrive;   // finalisation blocks done (reset by every producer)
+};
+
+DPZ_HD inline int64_t segments_per_chunk(int64_t C) { return (C + kSegment - 1) / kSegment; }
+
+inline size_t ws_bytes_for(int64_t P, int N)
+{
+    const int64_t segs = int64_t(N) * segments_per_chunk(P / N);
+    size_t b = kWsHeaderBytes + sizeof(double) * (size_t(kFinalBlocks) + size_t(segs));
+    return (b + 255) / 256 * 256;
+}
+
+inline double* ws_stage1(void* ws)
+{
+    return reinterpret_cast<double*>(static_cast<char*>(ws) + kWsHeaderBytes);
+}
+
+inline double* ws_partials(void* ws) { return ws_stage1(ws) + kFinalBlocks; }
+
+// One arena: N slabs of P elements, chunk C = P / N.
+struct Arena {
+    int64_t P;
+    int64_t C;
+    int N;
+    int gdt;   // 0 = fp32, 1 = bf16
+    int wdt;
+};
+
+// Divisor data for the average R(acc / N).
+struct Avg {
+    float fN;      // (float)N
+    float invN;    // 1/N, exact when N is a power of two
+    int pow2;      // multiply by invN (same result as dividing) when set
+};
+
+// AdamW constants, computed once on the host.
+struct AdamArgs {
+    float lr, b1, b2, omb1, omb2, bc1, bc2, eps, wd;
+    float clip;    // > 0: scale by clip/norm when norm > clip
+};
+
+// Which source the AdamW kernel reads the averaged gradient from.
+enum class AdamSrc { kLoadOwner, kFold };
+
+// Kernel launchers.  Each launches exactly one kernel on `s` and returns the
+// launch status.  Kernels that produce norm partials write one per
+// 256-element segment of every chunk (N * segments_per_chunk(C) in chunk
+// order), independent of their launch configuration, so the norm is a
+// function of the data alone.
+cudaError_t launch_reduce(const Arena& a, const Avg& avg, void* grads, bool all_slabs,
+                          void* ws, cudaStream_t s);
+cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaStream_t s);
+cudaError_t launch_norm_finalize(const Arena& a, void* ws, float* norm_out, cudaStream_t s);
+cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
+                         bool bcast, bool store_avg, void* grads, float* master, float* m,
+                         float* v, void* weights, void* ws, cudaStream_t s);
+cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
+
+// Name of the kernel the last launcher call on this thread launched.
+const char* last_kernel_name();
+void set_last_kernel_name(const char* name);
+
+// Blocks for a grid-stride kernel: one resident wave (SMs x resident blocks
+// per SM), fewer when `threads_needed` is smaller, at most `cap` if cap > 0.
+int grid_for(const void* kernel, int64_t threads_needed, int cap);
+
+}  // namespace dpz

@@ -1,0 +1,281 @@
+// Reduce-side kernels: ring-order reduce-scatter + average (optionally with
+// norm partials, optionally written back into every slab = all-reduce),
+// the norm of the owner chunks, its finalisation, and the all-gather.
+//
+// All streaming kernels use the same mapping: chunk-major, and inside chunk c
+// a grid-stride loop over 8-element groups, so every thread of a warp works on
+// the same chunk (uniform ring order) and consecutive threads touch
+// consecutive 16-byte words of every slab (coalesced).
+#include <mutex>
+#include <unordered_map>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace dpz {
+
+namespace {
+
+thread_local const char* g_last_kernel = "";
+
+struct DevInfo {
+    int sms = 0;
+};
+
+std::mutex g_mu;
+std::unordered_map<int, DevInfo> g_dev;
+std::unordered_map<const void*, int> g_occ;   // kernel -> resident blocks per SM
+
+int device_sms()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_dev.find(dev);
+    if (it != g_dev.end()) return it->second.sms;
+    DevInfo d;
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (d.sms <= 0) d.sms = 1;
+    g_dev[dev] = d;
+    return d.sms;
+}
+
+int blocks_per_sm(const void* fn)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occ.find(fn);
+        if (it != g_occ.end()) return it->second;
+    }
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kBlock, 0) != cudaSuccess || nb < 1)
+        nb = 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_occ[fn] = nb;
+    return nb;
+}
+
+}  // namespace
+
+// One resident wave (SMs x blocks per SM), fewer if the chunk is short.
+int grid_for(const void* fn, int64_t threads_needed, int cap)
+{
+    int64_t g = (int64_t)device_sms() * blocks_per_sm(fn);
+    int64_t need = (threads_needed + kBlock - 1) / kBlock;
+    if (need < g) g = need;
+    if (cap > 0 && g > cap) g = cap;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+const char* last_kernel_name() { return g_last_kernel; }
+void set_last_kernel_name(const char* n) { g_last_kernel = n; }
+
+// ------------------------------------------------------------------ kernels
+//
+// Loop shape shared by the streaming kernels: for chunk c = 0..N-1, each warp
+// walks warp-iterations wb = first, first + stride, ... (32 consecutive
+// groups of 8 elements, all lanes together), lane l taking group wb + l.
+// Kernels that produce norm partials write, for every warp-iteration, the sum
+// of squares of its 256 averaged elements (fixed shuffle tree) into the slot
+// of that segment, so the partials do not depend on the grid.
+
+// Ring-order reduce + average of every chunk.  ALL = false: chunk c goes to
+// slab c only (reduce-scatter).  ALL = true: to every slab (all-reduce).
+// SUMSQ: per-segment sums of squares of the averages.
+template <int GDT, bool ALL, bool SUMSQ>
+__global__ void __launch_bounds__(kBlock)
+k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int N, Avg avg,
+         WsHeader* __restrict__ hdr, double* __restrict__ partials)
+{
+    constexpr int ES = Group<GDT>::kBytes;
+    const int64_t slab = P * ES;
+    const int64_t groups = C / kGroup;
+    const int64_t segs = segments_per_chunk(C);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
+    if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
+    for (int c = 0; c < N; ++c) {
+        for (int64_t wb = first; wb < groups; wb += stride) {
+            const int64_t gi = wb + lane;
+            float ss = 0.0f;
+            if (gi < groups) {
+                const int64_t off = (c * C + gi * kGroup) * ES;
+                float acc[8];
+                ring_fold<GDT>(grads, slab, off, c, N, acc);
+                average8<GDT>(acc, avg);
+                if (SUMSQ) ss = sumsq8(acc);
+                const typename Group<GDT>::Raw out = Group<GDT>::pack(acc);
+                if (ALL) {
+                    for (int r = 0; r < N; ++r) Group<GDT>::store_raw(grads + r * slab + off, out);
+                } else {
+                    Group<GDT>::store_raw(grads + c * slab + off, out);
+                }
+            }
+            if (SUMSQ) {
+                const double t = warp_sum((double)ss);
+                if (lane == 0) partials[c * segs + wb / 32] = t;
+            }
+        }
+    }
+}
+
+// Sums of squares of the owner chunks (chunk c of slab c), per segment.
+template <int GDT>
+__global__ void __launch_bounds__(kBlock)
+k_norm_owned(const char* __restrict__ grads, int64_t P, int64_t C, int N,
+             WsHeader* __restrict__ hdr, double* __restrict__ partials)
+{
+    constexpr int ES = Group<GDT>::kBytes;
+    const int64_t slab = P * ES;
+    const int64_t groups = C / kGroup;
+    const int64_t segs = segments_per_chunk(C);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
+    if (blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
+    for (int c = 0; c < N; ++c) {
+        for (int64_t wb = first; wb < groups; wb += stride) {
+            const int64_t gi = wb + lane;
+            float ss = 0.0f;
+            if (gi < groups) {
+                float x[8];
+                load_group<GDT>(grads + c * slab + (c * C + gi * kGroup) * ES, x);
+                ss = sumsq8(x);
+            }
+            const double t = warp_sum((double)ss);
+            if (lane == 0) partials[c * segs + wb / 32] = t;
+        }
+    }
+}
+
+// Sum of the n segment partials in a fixed order, independent of the device:
+// block b of F adds the contiguous range [b*L, (b+1)*L) (L = ceil(n/F)) into
+// stage1[b]; the last block to arrive (an arrival counter, not an ordering)
+// adds stage1[0..F-1] and writes sumsq, the norm and *norm_out.  No block
+// waits for another.
+__global__ void __launch_bounds__(kFinalThreads)
+k_norm_finalize(WsHeader* __restrict__ hdr, double* __restrict__ stage1,
+                const double* __restrict__ partials, int64_t n, float* __restrict__ norm_out)
+{
+    const int F = gridDim.x;
+    const int64_t L = (n + F - 1) / F;
+    const int64_t lo = (int64_t)blockIdx.x * L;
+    const int64_t hi = lo + L < n ? lo + L : n;
+    double v = 0.0;
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) v += partials[i];
+    v = block_sum(v);
+    __shared__ bool is_last;
+    if (threadIdx.x == 0) {
+        stage1[blockIdx.x] = v;
+        __threadfence();
+        const unsigned prev = atomicAdd(&hdr->arrive, 1u);
+        is_last = prev == (unsigned)(F - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    double w = 0.0;
+    for (int i = threadIdx.x; i < F; i += blockDim.x) w += __ldcg(&stage1[i]);
+    w = block_sum(w);
+    if (threadIdx.x == 0) {
+        const float nrm = __double2float_rn(__dsqrt_rn(w));
+        hdr->sumsq = w;
+        hdr->norm = nrm;
+        hdr->nparts = (uint32_t)n;
+        hdr->arrive = 0u;
+        if (norm_out) *norm_out = nrm;
+    }
+}
+
+// Chunk c of slab c -> chunk c of every other slab.
+template <int WDT>
+__global__ void __launch_bounds__(kBlock)
+k_allgather(char* __restrict__ w, int64_t P, int64_t C, int N)
+{
+    constexpr int ES = Group<WDT>::kBytes;
+    const int64_t slab = P * ES;
+    const int64_t groups = C / kGroup;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int c = 0; c < N; ++c) {
+        for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups;
+             gi += stride) {
+            const int64_t off = (c * C + gi * kGroup) * ES;
+            const typename Group<WDT>::Raw x = Group<WDT>::load_raw(w + c * slab + off);
+            for (int r = 0; r < N; ++r)
+                if (r != c) Group<WDT>::store_raw(w + r * slab + off, x);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+
+template <int GDT, bool ALL, bool SUMSQ>
+static cudaError_t reduce_t(const Arena& a, const Avg& avg, void* grads, void* ws, cudaStream_t s)
+{
+    auto fn = k_reduce<GDT, ALL, SUMSQ>;
+    const int grid = grid_for((const void*)fn, a.C / kGroup, 0);
+    set_last_kernel_name(ALL ? "dpz_allreduce_avg" : SUMSQ ? "dpz_rs_avg_sumsq" : "dpz_rs_avg");
+    fn<<<grid, kBlock, 0, s>>>(static_cast<char*>(grads), a.P, a.C, a.N, avg,
+                               static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const Arena& a, const Avg& avg, void* grads, bool all_slabs, void* ws,
+                          cudaStream_t s)
+{
+    const bool sumsq = ws != nullptr && !all_slabs;
+    if (a.gdt == 1) {
+        if (all_slabs) return reduce_t<1, true, false>(a, avg, grads, ws, s);
+        return sumsq ? reduce_t<1, false, true>(a, avg, grads, ws, s)
+                     : reduce_t<1, false, false>(a, avg, grads, ws, s);
+    }
+    if (all_slabs) return reduce_t<0, true, false>(a, avg, grads, ws, s);
+    return sumsq ? reduce_t<0, false, true>(a, avg, grads, ws, s)
+                 : reduce_t<0, false, false>(a, avg, grads, ws, s);
+}
+
+cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaStream_t s)
+{
+    set_last_kernel_name("dpz_norm_owned");
+    const char* g = static_cast<const char*>(grads);
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    if (a.gdt == 1) {
+        const int grid = grid_for((const void*)k_norm_owned<1>, a.C / kGroup, 0);
+        k_norm_owned<1><<<grid, kBlock, 0, s>>>(g, a.P, a.C, a.N, hdr, ws_partials(ws));
+    } else {
+        const int grid = grid_for((const void*)k_norm_owned<0>, a.C / kGroup, 0);
+        k_norm_owned<0><<<grid, kBlock, 0, s>>>(g, a.P, a.C, a.N, hdr, ws_partials(ws));
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finalize(const Arena& a, void* ws, float* norm_out, cudaStream_t s)
+{
+    set_last_kernel_name("dpz_norm_finalize");
+    const int64_t n = int64_t(a.N) * segments_per_chunk(a.C);
+    // blocks: a function of n only, so the summation order is fixed
+    int64_t F = (n + 2047) / 2048;
+    if (F > kFinalBlocks) F = kFinalBlocks;
+    if (F < 1) F = 1;
+    k_norm_finalize<<<(int)F, kFinalThreads, 0, s>>>(static_cast<WsHeader*>(ws), ws_stage1(ws),
+                                                     ws_partials(ws), n, norm_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s)
+{
+    set_last_kernel_name("dpz_allgather");
+    char* w = static_cast<char*>(weights);
+    if (a.wdt == 1) {
+        const int grid = grid_for((const void*)k_allgather<1>, a.C / kGroup, 0);
+        k_allgather<1><<<grid, kBlock, 0, s>>>(w, a.P, a.C, a.N);
+    } else {
+        const int grid = grid_for((const void*)k_allgather<0>, a.C / kGroup, 0);
+        k_allgather<0><<<grid, kBlock, 0, s>>>(w, a.P, a.C, a.N);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace dpz

@@ -1,0 +1,192 @@
+"""Thin ctypes binding of libdpz.so (include/dpz.h): argument marshalling only.
+
+Every function of the C-ABI is exposed under its own name.  Tensor arguments
+are torch CUDA tensors (device memory and streams come from PyTorch); the
+computation is entirely the library's own CUDA kernels.  If libdpz.so is
+missing, importing this module raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdpz.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "dpz.h")
+
+F32, BF16 = 0, 1
+OK, ERR_INVALID_ARG, ERR_ALIGN, ERR_CUDA = 0, 1, 2, 3
+MAX_RANKS = 64
+
+
+class DpzError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"dpz error {code}: {msg}")
+        self.code = code
+
+
+class AdamWCfg(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("step", ctypes.c_int64), ("clip_norm", ctypes.c_float),
+                ("store_avg", ctypes.c_int)]
+
+
+class KernelStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
+
+
+_VP = ctypes.c_void_p
+_FP = ctypes.c_void_p     # float* (device)
+
+_SIGS = {
+    "dpz_workspace_bytes": ([ctypes.c_int64, ctypes.c_int], ctypes.c_size_t),
+    "dp_reduce_scatter_avg": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _VP], ctypes.c_int),
+    "dp_allreduce_avg": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _VP], ctypes.c_int),
+    "dp_grad_global_norm": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _VP, _FP, _VP],
+                            ctypes.c_int),
+    "zero1_adamw_step": ([_VP, _FP, _FP, _FP, _VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                          ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _VP], ctypes.c_int),
+    "dp_allgather": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _VP], ctypes.c_int),
+    "dp_zero1_step": ([_VP, _FP, _FP, _FP, _VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                       ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _FP, _VP], ctypes.c_int),
+    "dpz_last_error": ([], ctypes.c_char_p),
+    "dpz_version": ([], ctypes.c_char_p),
+    "dpz_launch_count": ([], ctypes.c_int64),
+    "dpz_profile_start": ([ctypes.c_int], ctypes.c_int),
+    "dpz_profile_stop": ([ctypes.POINTER(KernelStat), ctypes.c_int,
+                          ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+}
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run gradient_reduction_zero_gb300.build.build() "
+            "(there is no CPU fallback)")
+    L = ctypes.CDLL(LIB_PATH)
+    for name, (args, res) in _SIGS.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = res
+    return L
+
+
+lib = _load()
+
+
+def header_symbols(path: str = HEADER) -> list[str]:
+    """Names of the functions include/dpz.h declares."""
+    text = open(path).read()
+    return re.findall(r"DPZ_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def _check(rc: int) -> None:
+    if rc != OK:
+        raise DpzError(rc, lib.dpz_last_error().decode())
+
+
+# ------------------------------------------------------------ tensor helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def make_cfg(lr, beta1, beta2, eps, weight_decay, step, clip_norm=0.0, store_avg=False) -> AdamWCfg:
+    return AdamWCfg(lr, beta1, beta2, eps, weight_decay, int(step), clip_norm, int(bool(store_avg)))
+
+
+def workspace(P: int, N: int, device=None):
+    """A device tensor of dpz_workspace_bytes(P, N) bytes."""
+    torch = _torch()
+    nb = lib.dpz_workspace_bytes(P, N)
+    if nb == 0:
+        raise DpzError(ERR_INVALID_ARG, f"no workspace size for P={P}, N={N}")
+    return torch.empty(nb, dtype=torch.uint8, device=device or "cuda")
+
+
+def _np(arena, N: int) -> int:
+    if arena.numel() % N:
+        raise ValueError("arena size is not a multiple of N")
+    return arena.numel() // N
+
+
+# ------------------------------------------------------------ the calls
+
+def dp_reduce_scatter_avg(grads, N: int, stream=None) -> None:
+    _check(lib.dp_reduce_scatter_avg(_ptr(grads), _np(grads, N), N, dtype_code(grads),
+                                     _stream_handle(stream)))
+
+
+def dp_allreduce_avg(grads, N: int, stream=None) -> None:
+    _check(lib.dp_allreduce_avg(_ptr(grads), _np(grads, N), N, dtype_code(grads),
+                                _stream_handle(stream)))
+
+
+def dp_grad_global_norm(grads, N: int, ws, norm_out=None, stream=None) -> None:
+    _check(lib.dp_grad_global_norm(_ptr(grads), _np(grads, N), N, dtype_code(grads), _ptr(ws),
+                                   _ptr(norm_out), _stream_handle(stream)))
+
+
+def zero1_adamw_step(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None,
+                     stream=None) -> None:
+    _check(lib.zero1_adamw_step(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
+                                _np(grads, N), N, dtype_code(grads), dtype_code(weights),
+                                ctypes.byref(cfg), _ptr(ws), _stream_handle(stream)))
+
+
+def dp_allgather(weights, N: int, stream=None) -> None:
+    _check(lib.dp_allgather(_ptr(weights), _np(weights, N), N, dtype_code(weights),
+                            _stream_handle(stream)))
+
+
+def dp_zero1_step(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None, norm_out=None,
+                  stream=None) -> None:
+    _check(lib.dp_zero1_step(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
+                             _np(grads, N), N, dtype_code(grads), dtype_code(weights),
+                             ctypes.byref(cfg), _ptr(ws), _ptr(norm_out),
+                             _stream_handle(stream)))
+
+
+def launch_count() -> int:
+    return int(lib.dpz_launch_count())
+
+
+def version() -> str:
+    return lib.dpz_version().decode()
+
+
+def profile_start(max_launches: int = 4096) -> None:
+    _check(lib.dpz_profile_start(max_launches))
+
+
+def profile_stop() -> dict:
+    """{kernel name: (launches, total_ms)} for the launches since profile_start."""
+    stats = (KernelStat * 64)()
+    n = ctypes.c_int()
+    _check(lib.dpz_profile_stop(stats, 64, ctypes.byref(n)))
+    return {stats[i].name.decode(): (int(stats[i].launches), float(stats[i].total_ms))
+            for i in range(min(n.value, 64))}

@@ -1,0 +1,193 @@
+/*
+ * dpz — the data-parallel / ZeRO-1 gradient-synchronisation and optimizer step
+ * for N simulated ranks whose replicas all live in one GPU's memory.
+ *
+ * A "rank" is a replica slab of an arena.  The collectives of the pages become
+ * in-memory kernels: a ring "send" of a chunk is a load from another slab, the
+ * ring's hop order is a fixed per-element fold order, and an all-gather is N
+ * coalesced stores.  Every call is asynchronous on the caller's CUDA stream,
+ * never synchronises the host, allocates nothing, and launches only this
+ * library's own kernels.
+ *
+ * ------------------------------------------------------------------------
+ * Layout (all buffers are owned and allocated by the caller, device memory)
+ *
+ *   N   number of ranks, 1 <= N <= 64
+ *   P   elements per replica (a flat parameter / gradient arena), P % (8N) == 0
+ *   C   chunk = shard = P / N; chunk c is elements [c*C, (c+1)*C)
+ *   grads    [N][P] gradient dtype: slab r = grads + r*P = rank r's gradients
+ *   weights  [N][P] weight dtype:   slab r = rank r's weight replica
+ *   master, m, v   [P] fp32 each: the N ranks' shards laid end to end, so rank
+ *            r's shard (A4 — Multi-GPU with NCCL and ZeRO-1, Part 2:
+ *            shard_offset = rank * shard_size) is elements [r*C, (r+1)*C)
+ *   ws       dpz_workspace_bytes(P, N) bytes, 16-byte aligned: norm partials
+ *            and the global norm, written and read only by this library
+ *
+ * Chunk ownership: rank c owns chunk c.  The reduce-scatter is the ring of
+ * "Lab 09 — Parallelism, simulated", §1, rotated so that its last receiver of
+ * chunk c is rank c; element i of chunk c is therefore summed as the left fold
+ *     acc = x[(c+1)%N][i];  acc = R(acc + x[(c+j)%N][i]) for j = 2..N
+ * where R rounds to the gradient dtype (identity for fp32; round to nearest
+ * even for bf16, so a bf16 ring rounds once per hop: 13.5 Multi-GPU from First
+ * Principles, Exercise 8).  The average is R(acc / N): sum, then divide by N
+ * (Lab 09 §2; A4 Part 3, ncclAvg).  The fold order never depends on the
+ * launch configuration, so results are bit-for-bit reproducible.
+ *
+ * Alignment: every base pointer 16-byte aligned, and C*(element bytes) a
+ * multiple of 16 (P % (8N) == 0 guarantees it for both dtypes).
+ *
+ * Status: every call returns DPZ_OK or an error code without launching
+ * anything when an argument is invalid (null pointer, N out of range,
+ * P <= 0, P % N != 0, bad dtype, step < 1, overlapping buffers), and
+ * DPZ_ERR_ALIGN for misaligned pointers or chunks.  A CUDA launch failure
+ * returns DPZ_ERR_CUDA.  dpz_last_error() gives the calling thread's last
+ * message.  NaN and Inf inputs are not special-cased: they propagate.
+ *
+ * Streams: the caller orders producers of `grads` before the call with
+ * events (A4 Part 3: record an event on the compute stream, make the
+ * communication stream wait on it), and consumers after it.
+ */
+#ifndef DPZ_H
+#define DPZ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DPZ_API __attribute__((visibility("default")))
+#else
+#define DPZ_API
+#endif
+
+/* element types */
+#define DPZ_F32 0
+#define DPZ_BF16 1
+
+/* status codes */
+#define DPZ_OK 0
+#define DPZ_ERR_INVALID_ARG 1
+#define DPZ_ERR_ALIGN 2
+#define DPZ_ERR_CUDA 3
+
+#define DPZ_MAX_RANKS 64
+
+/* AdamW hyperparameters for one step (A4 Part 4: the optimizer runs on the
+ * owned shard).  The update, in fp32 with every operation rounded:
+ *   g  = avg * s          s = clip/norm if clip_norm > 0 and norm > clip_norm,
+ *                         else 1 (norm: of the averaged gradient, before the
+ *                         step)
+ *   m  = beta1*m + (1-beta1)*g
+ *   v  = beta2*v + (1-beta2)*(g*g)
+ *   mh = m / bc1,  vh = v / bc2,  bc = 1 - beta^step (host, double -> float)
+ *   theta = theta - lr * (mh / (sqrt(vh) + eps) + weight_decay * theta)
+ * weights = theta cast to the weight dtype (round to nearest even for bf16). */
+typedef struct dpz_adamw_cfg {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay;
+    int64_t step;        /* t >= 1, passed by the caller; the library keeps no state */
+    float clip_norm;     /* > 0: global-norm clip to this value; <= 0: no clip */
+    int store_avg;       /* dp_zero1_step without clip: nonzero also stores the
+                            averaged gradient into chunk c of slab c */
+} dpz_adamw_cfg;
+
+/* Per-kernel timing collected while profiling is on (see dpz_profile_start). */
+typedef struct dpz_kernel_stat {
+    char name[48];
+    int64_t launches;
+    double total_ms;     /* sum of per-launch CUDA-event durations */
+} dpz_kernel_stat;
+
+/* Bytes of device workspace `ws` must provide for an arena of N slabs of P
+ * elements: a 256-byte header (the norm), 256 first-stage sums and one fp64
+ * sum of squares per 256-element segment of every chunk (about P/32 bytes).
+ * Returns 0 for invalid P or N. */
+DPZ_API size_t dpz_workspace_bytes(int64_t P, int N);
+
+/* Ring reduce-scatter + average, in place (A4 Part 3: ncclReduceScatter of
+ * pointers[i] into pointers[i] + shard_offset with ncclAvg; Lab 09 §1 ring).
+ * grads: [N][P] device, dtype gdtype.  On return chunk c of slab c holds the
+ * average of chunk c over the N ranks; every other chunk of every slab is
+ * untouched.  Reads N*P and writes P elements. */
+DPZ_API int dp_reduce_scatter_avg(void* grads, int64_t P, int N, int gdtype,
+                                  void* stream);
+
+/* Ring all-reduce + average (ZeRO-0), in place (A4 Part 3, zero_stage 0:
+ * ncclAllReduce with ncclAvg; Lab 09 §1: reduce-scatter then all-gather).
+ * On return every slab holds the average; chunk c equals what the
+ * reduce-scatter leaves in chunk c of slab c.  Reads and writes N*P. */
+DPZ_API int dp_allreduce_avg(void* grads, int64_t P, int N, int gdtype,
+                             void* stream);
+
+/* Global L2 norm of the averaged gradient held in the owner chunks (chunk c of
+ * slab c, as left by dp_reduce_scatter_avg): each rank's sum of squares of its
+ * shard, then the sum over ranks ("Distributed training", Gates: ZeRO stages
+ * differ from DDP only in the order the global norm is summed).  Squares are
+ * summed in fp32 over groups of 8 and in fp64 beyond, in an order fixed by P
+ * and N alone (one partial per 256-element segment), so every entry point and
+ * every launch configuration gives the same bits.
+ * Writes the norm into ws (for zero1_adamw_step) and, if norm_out is not
+ * NULL, to *norm_out (device pointer to one float). */
+DPZ_API int dp_grad_global_norm(const void* grads, int64_t P, int N, int gdtype,
+                                void* ws, float* norm_out, void* stream);
+
+/* Sharded AdamW (A4 Part 4, step 1: adamw_update on this rank's shard only).
+ * For every rank c: reads the averaged chunk c of slab c, updates master/m/v
+ * elements [c*C, (c+1)*C) and writes the cast weights into chunk c of slab c
+ * of `weights` only (the all-gather is dp_allgather).  If cfg->clip_norm > 0
+ * the clip scale uses the norm that dp_grad_global_norm left in ws (ws may be
+ * NULL otherwise).  gdtype/wdtype: DPZ_F32 or DPZ_BF16. */
+DPZ_API int zero1_adamw_step(const void* grads, float* master, float* m,
+                             float* v, void* weights, int64_t P, int N,
+                             int gdtype, int wdtype, const dpz_adamw_cfg* cfg,
+                             const void* ws, void* stream);
+
+/* All-gather (A4 Part 4, step 2: ncclAllGather of the updated shards; Lab 09
+ * §1 all-gather phase): chunk c of slab c is copied into chunk c of every
+ * other slab, in place.  Reads P and writes (N-1)*P elements. */
+DPZ_API int dp_allgather(void* weights, int64_t P, int N, int wdtype,
+                         void* stream);
+
+/* The whole ZeRO-1 step, fused: reduce-scatter + average -> (global norm and
+ * clip) -> AdamW on each rank's shard -> cast -> all-gather into all N weight
+ * slabs.  Bit-identical to calling dp_reduce_scatter_avg,
+ * dp_grad_global_norm (when clipping), zero1_adamw_step and dp_allgather in
+ * turn.  Without clipping it is one kernel that reads each gradient byte once
+ * and writes the averages only if cfg->store_avg; with clipping it is three
+ * (reduce + norm partials and averages store, norm finalize, AdamW + cast +
+ * broadcast), because the clip scale depends on every element.  norm_out
+ * (device, may be NULL) receives the global norm; ws is required when
+ * clipping or when norm_out is given. */
+DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v,
+                          void* weights, int64_t P, int N, int gdtype,
+                          int wdtype, const dpz_adamw_cfg* cfg, void* ws,
+                          float* norm_out, void* stream);
+
+/* The calling thread's last error message ("" if none). */
+DPZ_API const char* dpz_last_error(void);
+
+/* Library version string. */
+DPZ_API const char* dpz_version(void);
+
+/* Number of kernels this library has launched since it was loaded. */
+DPZ_API int64_t dpz_launch_count(void);
+
+/* Profiling: while on, every kernel launch is bracketed by a pair of CUDA
+ * events recorded on the launch's own stream (capacity: max_launches
+ * launches; later launches are not timed).  dpz_profile_stop synchronises
+ * those events, fills up to max_stats per-kernel totals, sets *n_stats and
+ * turns profiling off. */
+DPZ_API int dpz_profile_start(int max_launches);
+DPZ_API int dpz_profile_stop(dpz_kernel_stat* stats, int max_stats, int* n_stats);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DPZ_H */

@@ -1,0 +1,131 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments before any CUDA call."""
+import ctypes
+import importlib.util
+import os
+import subprocess
+import sys
+
+import pytest
+
+from conftest import ROOT
+
+
+def _build():
+    path = os.path.join(ROOT, "gradient_reduction_zero_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_dpz_build_t", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
+@pytest.fixture(scope="module")
+def dpz():
+    _build()
+    import gradient_reduction_zero_gb300.dpz as d
+    return d
+
+
+def test_header_declares_the_north_star_calls(dpz):
+    names = dpz.header_symbols()
+    for n in ("dp_reduce_scatter_avg", "dp_allreduce_avg", "dp_grad_global_norm",
+              "zero1_adamw_step", "dp_allgather", "dp_zero1_step", "dpz_workspace_bytes",
+              "dpz_last_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(dpz):
+    lib = ctypes.CDLL(dpz.LIB_PATH)
+    names = dpz.header_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_bytes(dpz):
+    # header + 256 first-stage sums + one double per 256-element segment
+    segs = 4 * ((1_557_611_200 // 4 + 255) // 256)
+    want = 256 + 8 * (256 + segs)
+    assert dpz.lib.dpz_workspace_bytes(1_557_611_200, 4) == (want + 255) // 256 * 256
+    assert dpz.lib.dpz_workspace_bytes(4096, 4) == (256 + 8 * (256 + 16) + 255) // 256 * 256
+    assert dpz.lib.dpz_workspace_bytes(4098, 4) == 0
+    assert dpz.lib.dpz_workspace_bytes(4096, 0) == 0
+
+
+A = 0x7F0000000000          # fake, 16-byte aligned device addresses (never touched)
+MB = 1 << 20
+
+
+def _cfg(dpz, step=1, clip=0.0):
+    return dpz.make_cfg(1e-3, 0.9, 0.999, 1e-8, 0.1, step, clip)
+
+
+def _step(dpz, grads=A, master=A + 64 * MB, m=A + 80 * MB, v=A + 96 * MB,
+          weights=A + 112 * MB, P=4096, N=4, g=0, w=1, cfg=None, ws=A + 200 * MB, norm=None):
+    cfg = cfg or _cfg(dpz)
+    return dpz.lib.dp_zero1_step(grads, master, m, v, weights, P, N, g, w, ctypes.byref(cfg),
+                                 ws, norm, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(grads=None), 1),
+    (dict(master=None), 1),
+    (dict(weights=None), 1),
+    (dict(N=0), 1),
+    (dict(N=65), 1),
+    (dict(P=0), 1),
+    (dict(P=-8), 1),
+    (dict(P=4098), 1),                  # P % N != 0
+    (dict(P=4 * 1028), 2),              # chunk 1028 not a multiple of 8
+    (dict(grads=A + 8), 2),             # misaligned
+    (dict(m=A + 80 * MB + 4), 2),
+    (dict(g=2), 1),                     # unknown dtype
+    (dict(w=-1), 1),
+    (dict(m=A + 64 * MB + 8192), 1),    # m overlaps master
+    (dict(weights=A + 32 * 1024), 1),   # weights overlap grads (4*4096*4 bytes)
+])
+def test_zero1_step_rejects(dpz, kw, code):
+    assert _step(dpz, **kw) == code
+    assert dpz.lib.dpz_last_error().decode() != ""
+
+
+def test_zero1_step_rejects_bad_step_and_missing_ws(dpz):
+    assert _step(dpz, cfg=_cfg(dpz, step=0)) == 1
+    assert b"step" in dpz.lib.dpz_last_error()
+    # clipping needs the workspace
+    assert _step(dpz, cfg=_cfg(dpz, clip=1.0), ws=None) == 1
+    # ... but ws overlapping the weights is refused
+    assert _step(dpz, cfg=_cfg(dpz, clip=1.0), ws=A + 112 * MB + 16) == 1
+
+
+def test_other_calls_reject(dpz):
+    L = dpz.lib
+    assert L.dp_reduce_scatter_avg(None, 4096, 4, 0, None) == 1
+    assert L.dp_reduce_scatter_avg(A, 4096, 4, 7, None) == 1
+    assert L.dp_reduce_scatter_avg(A + 4, 4096, 4, 0, None) == 2
+    assert L.dp_allreduce_avg(A, 4096, 3, 0, None) == 1          # 4096 % 3
+    assert L.dp_allreduce_avg(A, 12, 3, 0, None) == 2            # chunk 4
+    assert L.dp_allgather(A, 4096, 0, 1, None) == 1
+    assert L.dp_grad_global_norm(A, 4096, 4, 1, None, None, None) == 1
+    assert L.dp_grad_global_norm(A, 4096, 4, 1, A + 100, None, None) == 2
+    assert L.dp_grad_global_norm(A, 4096, 4, 1, A + 64, None, None) == 1   # ws inside grads
+    cfg = _cfg(dpz)
+    assert L.zero1_adamw_step(A, None, A + MB, A + 2 * MB, A + 3 * MB, 4096, 4, 0, 0,
+                              ctypes.byref(cfg), None, None) == 1
+    assert L.zero1_adamw_step(A, A + MB, A + 2 * MB, A + 3 * MB, A + 4 * MB, 4096, 4, 0, 0,
+                              None, None, None) == 1
+    assert L.dpz_profile_start(0) == 1
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """The binding has no fallback: with libdpz.so absent, import raises."""
+    pkg = tmp_path / "gradient_reduction_zero_gb300"
+    pkg.mkdir()
+    src = os.path.join(ROOT, "gradient_reduction_zero_gb300", "dpz.py")
+    (pkg / "dpz.py").write_text(open(src).read())
+    (pkg / "__init__.py").write_text("")
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "try:\n    import gradient_reduction_zero_gb300.dpz\n"
+            "except ImportError as e:\n    print('raised', e)\n" % str(tmp_path))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
+    assert "raised" in out.stdout and "no CPU fallback" in out.stdout

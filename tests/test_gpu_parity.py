@@ -1,0 +1,305 @@
+"""GPU parity: every entry point of the C-ABI against the CPU oracle on the same
+seeded inputs, at sizes that span several grid-stride tiles with a ragged
+tail, plus the edge cases (N = 1, minimal chunks, NaN/Inf, subnormals,
+non-power-of-two N, N up to 64)."""
+import numpy as np
+import pytest
+import torch
+
+import inputs as I
+import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import gradient_reduction_zero_gb300.dpz as dpz
+    from gpu_util import (DEV, assert_close_tol, assert_weights, down, f32_view, np_dtype,
+                          same_bits, state_tolerances, up)
+
+# (N, C): C = chunk elements.  2048 elements = one block-iteration of a
+# 256-thread block; C = 3_000_016 makes every thread loop several times.
+SHAPES = [(1, 8), (1, 4104), (2, 8), (2, 2056), (3, 1000), (4, 1024), (4, 6152),
+          (5, 2000), (7, 776), (8, 12344), (16, 520), (64, 72), (4, 3_000_016)]
+
+
+def rand_grads(N, C, gdt, seed, sigma=1.0):
+    w = I.TINY.with_(N=N, P=N * C, gdtype=gdt, grad=I.Dist(I.NORMAL, sigma), grad_seed=seed)
+    return I.arena_host(w)
+
+
+def oracle_rs(g):
+    a = g.copy()
+    O.ring_reduce_scatter(a)
+    O.average_owned(a)
+    return a
+
+
+# ----------------------------------------------------------- reduce-scatter
+
+@pytest.mark.parametrize("N,C", SHAPES)
+@pytest.mark.parametrize("gdt", ["f32", "bf16"])
+def test_reduce_scatter_avg(N, C, gdt):
+    g = rand_grads(N, C, gdt, seed=N * 100 + C % 97)
+    ref = oracle_rs(g)
+    G = up(g)
+    dpz.dp_reduce_scatter_avg(G, N)
+    out = down(G)
+    for c in range(N):
+        for r in range(N):
+            sl = slice(c * C, (c + 1) * C)
+            want = ref[c, sl] if r == c else g[r, sl]       # other chunks untouched
+            assert same_bits(out[r, sl], want), (r, c)
+
+
+@pytest.mark.parametrize("N,C", SHAPES)
+@pytest.mark.parametrize("gdt", ["f32", "bf16"])
+def test_allreduce_avg(N, C, gdt):
+    g = rand_grads(N, C, gdt, seed=7 + N)
+    ref = g.copy()
+    O.ring_allreduce_avg(ref)
+    G = up(g)
+    dpz.dp_allreduce_avg(G, N)
+    assert same_bits(down(G), ref)
+
+
+@pytest.mark.parametrize("N,C", [(1, 8), (2, 2056), (4, 6152), (8, 776), (64, 72)])
+@pytest.mark.parametrize("wdt", ["f32", "bf16"])
+def test_allgather(N, C, wdt):
+    w = rand_grads(N, C, wdt, seed=3)
+    ref = w.copy()
+    O.ring_allgather(ref)
+    W = up(w)
+    dpz.dp_allgather(W, N)
+    assert same_bits(down(W), ref)
+
+
+# ----------------------------------------------------------- norm
+
+@pytest.mark.parametrize("N,C", [(1, 8), (3, 1000), (4, 6152), (8, 12344), (4, 3_000_016)])
+@pytest.mark.parametrize("gdt", ["f32", "bf16"])
+def test_global_norm(N, C, gdt):
+    g = rand_grads(N, C, gdt, seed=11 * N, sigma=1e-3)
+    ref = oracle_rs(g)
+    onorm, _ = O.clip_scale(O.sumsq_owned(ref), 0.0)
+    G = up(g)
+    ws = dpz.workspace(N * C, N, DEV)
+    nrm = torch.zeros(1, device=DEV)
+    dpz.dp_reduce_scatter_avg(G, N)
+    dpz.dp_grad_global_norm(G, N, ws, nrm)
+    gn = nrm.item()
+    assert abs(gn - onorm) <= 1e-6 * onorm
+
+
+# ----------------------------------------------------------- the step
+
+def make_problem(N, C, gdt, wdt, clip, seed, step=1000, gsigma=1e-3):
+    w = I.TINY.with_(N=N, P=N * C, gdtype=gdt, wdtype=wdt, clip=clip,
+                     grad=I.Dist(I.NORMAL_TAIL, gsigma), grad_seed=seed,
+                     m=I.Dist(I.NORMAL, 1e-4), v=I.Dist(I.ABS_NORMAL, 1e-6),
+                     lr=1.5e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=step)
+    g = I.arena_host(w)
+    th, m, v = (I.state_host(w, k) for k in ("master", "m", "v"))
+    wts = np.full((N, w.P), 0x7F7F if wdt == "bf16" else 3.0, dtype=np_dtype(wdt))
+    return w, g, th, m, v, wts
+
+
+def run_gpu_step(w, g, th, m, v, wts, store_avg=True, want_norm=True, fused=True):
+    G, T, M, V, W = up(g), up(th), up(m), up(v), up(wts)
+    ws = dpz.workspace(w.P, w.N, DEV)
+    nrm = torch.full((1,), -1.0, device=DEV)
+    cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip,
+                       store_avg=store_avg)
+    if fused:
+        dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm if want_norm else None)
+    else:
+        dpz.dp_reduce_scatter_avg(G, w.N)
+        if w.clip > 0 or want_norm:
+            dpz.dp_grad_global_norm(G, w.N, ws, nrm)
+        dpz.zero1_adamw_step(G, T, M, V, W, w.N, cfg, ws=ws)
+        dpz.dp_allgather(W, w.N)
+    torch.cuda.synchronize()
+    return down(G), down(T), down(M), down(V), down(W), nrm.item()
+
+
+def check_step(w, g, th, m, v, wts, out, check_avg=True):
+    Gg, Tg, Mg, Vg, Wg, gnorm = out
+    cfg = O.cfg_from_workload(w)
+    G, T, M, V, W = g.copy(), th.copy(), m.copy(), v.copy(), wts.copy()
+    onorm, oscale, _, _ = O.zero1_step(G, T, M, V, W, cfg)
+    C = w.C
+    if gnorm >= 0:
+        assert abs(gnorm - onorm) <= 1e-6 * onorm, (gnorm, onorm)
+    if check_avg:
+        for c in range(w.N):
+            sl = slice(c * C, (c + 1) * C)
+            assert same_bits(Gg[c, sl], G[c, sl]), f"averaged chunk {c}"
+    exact = w.clip <= 0 or gnorm == onorm
+    if exact:
+        assert same_bits(Tg, T) and same_bits(Mg, M) and same_bits(Vg, V)
+        assert same_bits(Wg, W)
+        return
+    avg = np.concatenate([f32_view(G[c, c * C:(c + 1) * C]) for c in range(w.N)])
+    tm, tv, tt = state_tolerances(avg, oscale, th, m, v, M, V, cfg)
+    assert_close_tol(Mg, M, tm, "m")
+    assert_close_tol(Vg, V, tv, "v")
+    assert_close_tol(Tg, T, tt, "master")
+    if Wg.dtype == np.uint16:
+        assert_weights(Wg, W, exact=False)
+    else:
+        for r in range(w.N):
+            assert_close_tol(Wg[r], W[r], tt, "weights")
+
+
+STEP_SHAPES = [(1, 8), (1, 4104), (2, 2056), (3, 1000), (4, 1024), (4, 6152), (5, 2000),
+               (8, 12344), (16, 520), (64, 72), (4, 3_000_016)]
+
+
+@pytest.mark.parametrize("N,C", STEP_SHAPES)
+@pytest.mark.parametrize("gdt,wdt", [("bf16", "bf16"), ("f32", "bf16"), ("f32", "f32"),
+                                     ("bf16", "f32")])
+@pytest.mark.parametrize("clip", [0.0, 1e-3])
+def test_zero1_step(N, C, gdt, wdt, clip):
+    w, g, th, m, v, wts = make_problem(N, C, gdt, wdt, clip, seed=N + C % 13)
+    out = run_gpu_step(w, g, th, m, v, wts)
+    check_step(w, g, th, m, v, wts, out)
+
+
+@pytest.mark.parametrize("N,C", [(4, 6152), (8, 776), (3, 1000)])
+@pytest.mark.parametrize("clip", [0.0, 1e-3])
+def test_fused_equals_unfused(N, C, clip):
+    """dp_zero1_step is bit-identical to the four separate calls."""
+    w, g, th, m, v, wts = make_problem(N, C, "bf16", "bf16", clip, seed=5)
+    a = run_gpu_step(w, g, th, m, v, wts, fused=True)
+    b = run_gpu_step(w, g, th, m, v, wts, fused=False)
+    for x, y in zip(a[:5], b[:5]):
+        assert same_bits(x, y)
+    assert a[5] == b[5]
+
+
+@pytest.mark.parametrize("store_avg,want_norm", [(False, False), (False, True), (True, False)])
+def test_no_clip_variants(store_avg, want_norm):
+    N, C = 4, 6152
+    w, g, th, m, v, wts = make_problem(N, C, "bf16", "bf16", 0.0, seed=9)
+    out = run_gpu_step(w, g, th, m, v, wts, store_avg=store_avg, want_norm=want_norm)
+    Gg = out[0]
+    if not store_avg:
+        assert same_bits(Gg, g)          # gradients left as they were
+    if not want_norm:
+        assert out[5] == -1.0
+    check_step(w, g, th, m, v, wts, out, check_avg=store_avg)
+
+
+def test_deterministic():
+    w, g, th, m, v, wts = make_problem(8, 12344, "bf16", "bf16", 1e-3, seed=1)
+    a = run_gpu_step(w, g, th, m, v, wts)
+    b = run_gpu_step(w, g, th, m, v, wts)
+    for x, y in zip(a[:5], b[:5]):
+        assert same_bits(x, y)
+    assert a[5] == b[5]
+
+
+def test_multi_step_matches_oracle():
+    """Three consecutive steps (t = 1, 2, 3) from m = v = 0."""
+    N, C = 4, 2056
+    w, g, th, m, v, wts = make_problem(N, C, "bf16", "bf16", 0.0, seed=2, step=1)
+    m[:] = 0
+    v[:] = 0
+    G, T, M, V, W = up(g), up(th), up(m), up(v), up(wts)
+    To, Mo, Vo, Wo = th.copy(), m.copy(), v.copy(), wts.copy()
+    for t in (1, 2, 3):
+        wt = w.with_(step=t)
+        gt = I.arena_host(wt.with_(grad_seed=10 * t))
+        G.copy_(up(gt))
+        cfg = dpz.make_cfg(wt.lr, wt.beta1, wt.beta2, wt.eps, wt.weight_decay, t, 0.0)
+        dpz.dp_zero1_step(G, T, M, V, W, N, cfg)
+        O.zero1_step(gt.copy(), To, Mo, Vo, Wo, O.cfg_from_workload(wt))
+    torch.cuda.synchronize()
+    assert same_bits(down(T), To) and same_bits(down(M), Mo) and same_bits(down(V), Vo)
+    assert same_bits(down(W), Wo)
+
+
+# ----------------------------------------------------------- edge cases
+
+def test_nan_inf_propagate():
+    N, C = 4, 1024
+    w, g, th, m, v, wts = make_problem(N, C, "f32", "bf16", 0.0, seed=3)
+    g[1, 5] = np.nan
+    g[2, C + 7] = np.inf
+    g[0, 2 * C + 9] = -np.inf
+    g[3, 2 * C + 9] = np.inf          # inf - inf = NaN in the fold
+    out = run_gpu_step(w, g, th, m, v, wts)
+    check_step(w, g, th, m, v, wts, out)
+    assert np.isnan(out[1][5]) and np.isnan(out[1][2 * C + 9])
+
+
+def test_subnormal_and_zero_gradients():
+    N, C = 4, 1024
+    w, g, th, m, v, wts = make_problem(N, C, "f32", "f32", 0.0, seed=4)
+    g[:, :C] = 0.0
+    g[:, C:2 * C] = np.float32(1e-41)          # subnormal; the average underflows further
+    g[:, 2 * C:2 * C + 8] = np.float32(-3e-45)
+    out = run_gpu_step(w, g, th, m, v, wts)
+    check_step(w, g, th, m, v, wts, out)
+    bg = O.f32_to_bf16(g)
+    out = run_gpu_step(w.with_(gdtype="bf16"), bg, th, m, v, wts)
+    check_step(w.with_(gdtype="bf16"), bg, th, m, v, wts, out)
+
+
+def test_guard_bands_untouched():
+    """Bytes just outside every buffer keep their canary values."""
+    N, C = 4, 2056
+    w, g, th, m, v, wts = make_problem(N, C, "bf16", "bf16", 1e-3, seed=6)
+    pad = 4096
+
+    def guarded(a):
+        flat = a.reshape(-1)
+        buf = np.full(flat.size + 2 * pad, 0x5A5A if a.dtype == np.uint16 else 1234.5,
+                      dtype=a.dtype)
+        buf[pad:pad + flat.size] = flat
+        return up(buf)
+
+    srcs = (g, th, m, v, wts)
+    bufs = [guarded(x) for x in srcs]
+    views = [b[pad:-pad].view(x.shape) for b, x in zip(bufs, srcs)]
+    ws = dpz.workspace(w.P, N, DEV)
+    cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)
+    dpz.dp_zero1_step(*views, N, cfg, ws=ws)
+    torch.cuda.synchronize()
+    for b, x in zip(bufs, srcs):
+        canary = 0x5A5A if x.dtype == np.uint16 else np.float32(1234.5)
+        hb = down(b)
+        assert np.all(hb[:pad] == canary) and np.all(hb[-pad:] == canary)
+
+
+def test_misaligned_tensor_is_refused():
+    g = torch.zeros(4 * 1024 + 1, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(dpz.DpzError) as e:
+        dpz.dp_reduce_scatter_avg(g[1:], 4)
+    assert e.value.code == dpz.ERR_ALIGN
+
+
+def test_device_generator_matches_host():
+    """The inputs the GPU tests and the bench generate on the device are the
+    oracle's inputs, bit for bit."""
+    for w in (I.GPT2_1P5B.with_(P=4 * 65536), I.TINY):
+        t = torch.empty(w.N * w.P, dtype=torch.bfloat16 if w.gdtype == "bf16" else torch.float32,
+                        device=DEV)
+        I.fill_grads_device(w, t)
+        for which in ("master", "m", "v"):
+            s = torch.empty(w.P, dtype=torch.float32, device=DEV)
+            I.fill_state_device(w, which, s)
+            assert np.array_equal(down(s), I.state_host(w, which))
+        torch.cuda.synchronize()
+        assert np.array_equal(down(t).reshape(w.N, w.P), I.arena_host(w))
+
+
+def test_profiling_and_launch_count():
+    N, C = 4, 6152
+    w, g, th, m, v, wts = make_problem(N, C, "bf16", "bf16", 1e-3, seed=8)
+    before = dpz.launch_count()
+    dpz.profile_start(64)
+    run_gpu_step(w, g, th, m, v, wts)
+    stats = dpz.profile_stop()
+    assert dpz.launch_count() - before == 3
+    assert set(stats) == {"dpz_rs_avg_sumsq", "dpz_norm_finalize", "dpz_adamw_bcast"}
+    assert all(n == 1 and ms > 0 for n, ms in stats.values())
