@@ -8,13 +8,16 @@
 
 namespace dpz {
 
-template <int GDT, int WDT, bool FOLD, bool BCAST, bool SUMSQ>
+// NT > 0: N == NT known at compile time (the fold and the broadcast unroll);
+// NT == 0: any N, read from n_rt.
+template <int GDT, int WDT, int NT, bool FOLD, bool BCAST, bool SUMSQ>
 __global__ void __launch_bounds__(kBlock)
 k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
-        float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int N,
+        float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int n_rt,
         Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
         double* __restrict__ partials)
 {
+    const int N = NT > 0 ? NT : n_rt;
     constexpr int GES = Group<GDT>::kBytes;
     constexpr int WES = Group<WDT>::kBytes;
     const int64_t gslab = P * GES;
@@ -38,6 +41,9 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
     const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
     if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     for (int c = 0; c < N; ++c) {
+        constexpr int NS = NT > 0 ? NT : 1;
+        const char* src[NS];
+        if constexpr (NT > 0) ring_sources<NT>(grads, gslab, c, src);
         for (int64_t wb = first; wb < groups; wb += stride) {
             const int64_t gi = wb + lane;
             float ss = 0.0f;
@@ -45,7 +51,15 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
                 const int64_t e = c * C + gi * kGroup;  // element index (same in every slab)
                 float g[8];
                 if (FOLD) {
-                    ring_fold<GDT>(grads, gslab, e * GES, c, N, g);
+                    if constexpr (NT > 0) {
+                        typename Group<GDT>::Raw raw[NT];
+#pragma unroll
+                        for (int j = 0; j < NT; ++j)
+                            raw[j] = Group<GDT>::load_raw(src[j] + e * GES);
+                        fold_loaded<GDT, NT>(raw, g);
+                    } else {
+                        ring_fold<GDT>(grads, gslab, e * GES, c, N, g);
+                    }
                     average8<GDT>(g, avg);
                     if (SUMSQ) ss = sumsq8(g);
                     if (store_avg) store_group<GDT>(grads + c * gslab + e * GES, g);
@@ -66,27 +80,35 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
                 store_group<0>(reinterpret_cast<char*>(var + e), vv);
                 const typename Group<WDT>::Raw w = Group<WDT>::pack(th);
                 if (BCAST) {
-                    for (int r = 0; r < N; ++r)
-                        Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
+                    if constexpr (NT > 0) {
+#pragma unroll
+                        for (int r = 0; r < NT; ++r)
+                            Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
+                    } else {
+                        for (int r = 0; r < N; ++r)
+                            Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
+                    }
                 } else {
                     Group<WDT>::store_raw(weights + c * wslab + e * WES, w);
                 }
             }
-            if (SUMSQ) {
-                const double t = warp_sum((double)ss);
-                if (lane == 0) partials[c * segs + wb / 32] = t;
+            if (SUMSQ) {                      // wb < groups: uniform over the warp
+                const float t = warp_sum_f32(ss);
+                if (lane == 0) partials[c * segs + wb / 32] = (double)t;
             }
         }
     }
 }
 
-template <int GDT, int WDT, bool FOLD, bool BCAST, bool SUMSQ>
+template <int GDT, int WDT, int NT, bool FOLD, bool BCAST, bool SUMSQ>
 static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
                            void* grads, float* master, float* m, float* v, void* weights,
                            void* ws, cudaStream_t s)
 {
-    auto fn = k_adamw<GDT, WDT, FOLD, BCAST, SUMSQ>;
-    const int grid = grid_for((const void*)fn, a.C / kGroup, 0);
+    auto fn = k_adamw<GDT, WDT, NT, FOLD, BCAST, SUMSQ>;
+    // the load-owner kernel balances better with blocks that replace early
+    // finishers; the fold kernel is register-heavier and keeps two waves
+    const int grid = grid_for((const void*)fn, a.C / kGroup, 0, FOLD ? 2 : 4);
     set_last_kernel_name(FOLD ? (SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused")
                               : (BCAST ? "dpz_adamw_bcast" : "dpz_adamw_owner"));
     fn<<<grid, kBlock, 0, s>>>(static_cast<char*>(grads), master, m, v,
@@ -96,6 +118,30 @@ static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bo
     return cudaGetLastError();
 }
 
+template <int GDT, int WDT, bool SUMSQ>
+static cudaError_t fused_n(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
+                           void* grads, float* master, float* m, float* v, void* weights,
+                           void* ws, cudaStream_t s)
+{
+    switch (a.N) {
+    case 1:
+        return adamw_t<GDT, WDT, 1, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                      weights, ws, s);
+    case 2:
+        return adamw_t<GDT, WDT, 2, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                      weights, ws, s);
+    case 4:
+        return adamw_t<GDT, WDT, 4, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                      weights, ws, s);
+    case 8:
+        return adamw_t<GDT, WDT, 8, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                      weights, ws, s);
+    default:
+        return adamw_t<GDT, WDT, 0, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                      weights, ws, s);
+    }
+}
+
 template <int GDT, int WDT>
 static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                             bool bcast, bool store_avg, void* grads, float* master, float* m,
@@ -103,16 +149,15 @@ static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, A
 {
     if (src == AdamSrc::kFold) {
         if (ws != nullptr)
-            return adamw_t<GDT, WDT, true, true, true>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s);
-        return adamw_t<GDT, WDT, true, true, false>(a, avg, h, store_avg, grads, master, m, v,
-                                                   weights, ws, s);
+            return fused_n<GDT, WDT, true>(a, avg, h, store_avg, grads, master, m, v, weights, ws,
+                                           s);
+        return fused_n<GDT, WDT, false>(a, avg, h, store_avg, grads, master, m, v, weights, ws, s);
     }
     if (bcast)
-        return adamw_t<GDT, WDT, false, true, false>(a, avg, h, false, grads, master, m, v,
+        return adamw_t<GDT, WDT, 0, false, true, false>(a, avg, h, false, grads, master, m, v,
+                                                       weights, ws, s);
+    return adamw_t<GDT, WDT, 0, false, false, false>(a, avg, h, false, grads, master, m, v,
                                                     weights, ws, s);
-    return adamw_t<GDT, WDT, false, false, false>(a, avg, h, false, grads, master, m, v, weights,
-                                                 ws, s);
 }
 
 cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,

@@ -70,11 +70,14 @@ int check_dtype(int dt, const char* what)
     return DPZ_OK;
 }
 
-int check_ptr(const void* p, const char* what)
+// bf16 buffers must be 16-byte aligned, fp32 buffers 32-byte aligned (the
+// kernels move 8 elements per lane in one 128- or 256-bit access).
+int check_ptr(const void* p, const char* what, int dt = DPZ_BF16)
 {
     if (p == nullptr) return fail(DPZ_ERR_INVALID_ARG, "%s is NULL", what);
-    if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
-        return fail(DPZ_ERR_ALIGN, "%s is not 16-byte aligned", what);
+    const uintptr_t align = dt == DPZ_F32 ? 32 : 16;
+    if (reinterpret_cast<uintptr_t>(p) % align != 0)
+        return fail(DPZ_ERR_ALIGN, "%s is not %d-byte aligned", what, (int)align);
     return DPZ_OK;
 }
 
@@ -203,7 +206,7 @@ DPZ_API int dp_reduce_scatter_avg(void* grads, int64_t P, int N, int gdtype, voi
 {
     DPZ_TRY(check_dims(P, N));
     DPZ_TRY(check_dtype(gdtype, "gradient"));
-    DPZ_TRY(check_ptr(grads, "grads"));
+    DPZ_TRY(check_ptr(grads, "grads", gdtype));
     const Arena a = make_arena(P, N, gdtype, gdtype);
     const Avg avg = make_avg(N);
     DPZ_TRY(launch(as_stream(stream), [&] {
@@ -216,7 +219,7 @@ DPZ_API int dp_allreduce_avg(void* grads, int64_t P, int N, int gdtype, void* st
 {
     DPZ_TRY(check_dims(P, N));
     DPZ_TRY(check_dtype(gdtype, "gradient"));
-    DPZ_TRY(check_ptr(grads, "grads"));
+    DPZ_TRY(check_ptr(grads, "grads", gdtype));
     const Arena a = make_arena(P, N, gdtype, gdtype);
     const Avg avg = make_avg(N);
     DPZ_TRY(launch(as_stream(stream), [&] {
@@ -230,7 +233,7 @@ DPZ_API int dp_grad_global_norm(const void* grads, int64_t P, int N, int gdtype,
 {
     DPZ_TRY(check_dims(P, N));
     DPZ_TRY(check_dtype(gdtype, "gradient"));
-    DPZ_TRY(check_ptr(grads, "grads"));
+    DPZ_TRY(check_ptr(grads, "grads", gdtype));
     DPZ_TRY(check_ptr(ws, "ws"));
     std::vector<Range> rs = {range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
                              range("ws", ws, (int64_t)dpz_workspace_bytes(P, N))};
@@ -252,11 +255,11 @@ static int check_step_buffers(const void* grads, const float* master, const floa
     DPZ_TRY(check_dtype(gdtype, "gradient"));
     DPZ_TRY(check_dtype(wdtype, "weight"));
     DPZ_TRY(check_cfg(cfg));
-    DPZ_TRY(check_ptr(grads, "grads"));
-    DPZ_TRY(check_ptr(master, "master"));
-    DPZ_TRY(check_ptr(m, "m"));
-    DPZ_TRY(check_ptr(v, "v"));
-    DPZ_TRY(check_ptr(weights, "weights"));
+    DPZ_TRY(check_ptr(grads, "grads", gdtype));
+    DPZ_TRY(check_ptr(master, "master", DPZ_F32));
+    DPZ_TRY(check_ptr(m, "m", DPZ_F32));
+    DPZ_TRY(check_ptr(v, "v", DPZ_F32));
+    DPZ_TRY(check_ptr(weights, "weights", wdtype));
     if (need_ws) DPZ_TRY(check_ptr(ws, "ws"));
     std::vector<Range> rs = {range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
                              range("master", master, P * 4), range("m", m, P * 4),
@@ -290,7 +293,7 @@ DPZ_API int dp_allgather(void* weights, int64_t P, int N, int wdtype, void* stre
 {
     DPZ_TRY(check_dims(P, N));
     DPZ_TRY(check_dtype(wdtype, "weight"));
-    DPZ_TRY(check_ptr(weights, "weights"));
+    DPZ_TRY(check_ptr(weights, "weights", wdtype));
     const Arena a = make_arena(P, N, wdtype, wdtype);
     cudaStream_t s = as_stream(stream);
     DPZ_TRY(launch(s, [&] { return launch_allgather(a, weights, s); }));

@@ -13,15 +13,48 @@
 namespace dpz {
 
 // ------------------------------------------------------------ memory access
+//
+// Every stream is touched once, so loads ask L2 to fetch whole 256-byte
+// segments (the next lanes' data) and skip L1, and stores are marked
+// evict-first.  fp32 streams use 256-bit accesses (sm_100 and later;
+// 32-byte aligned), bf16 streams 128-bit ones.
 
-__device__ __forceinline__ uint4 ld_stream(const void* p)
+struct U8 {
+    uint32_t x[8];
+};
+
+__device__ __forceinline__ uint4 ld16(const void* p)
 {
-    return __ldcs(reinterpret_cast<const uint4*>(p));
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
 }
 
-__device__ __forceinline__ void st_stream(void* p, uint4 v)
+__device__ __forceinline__ U8 ld32(const void* p)
 {
-    __stcs(reinterpret_cast<uint4*>(p), v);
+    U8 r;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.x[0]), "=r"(r.x[1]), "=r"(r.x[2]), "=r"(r.x[3]), "=r"(r.x[4]),
+                   "=r"(r.x[5]), "=r"(r.x[6]), "=r"(r.x[7])
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st16(void* p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st32(void* p, const U8& v)
+{
+    asm volatile("st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.x[0]),
+                 "r"(v.x[1]), "r"(v.x[2]), "r"(v.x[3]), "r"(v.x[4]), "r"(v.x[5]), "r"(v.x[6]),
+                 "r"(v.x[7])
+                 : "memory");
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -40,8 +73,17 @@ __device__ __forceinline__ float round_bf16(float x)
     return __bfloat162float(__float2bfloat16_rn(x));
 }
 
-// A group of 8 elements of one storage type.  DT 0 = fp32 (two 16-byte
-// words), DT 1 = bf16 (one 16-byte word).
+// Round two floats to bf16 (nearest even) with one paired conversion and
+// return them as floats again.
+__device__ __forceinline__ void round_bf16x2(float& lo, float& hi)
+{
+    const uint32_t w = pack_bf16x2(lo, hi);
+    lo = bf16_lo(w);
+    hi = bf16_hi(w);
+}
+
+// A group of 8 elements of one storage type.  DT 0 = fp32 (one 32-byte
+// word), DT 1 = bf16 (one 16-byte word).
 template <int DT>
 struct Group;
 
@@ -49,8 +91,8 @@ template <>
 struct Group<1> {
     static constexpr int kBytes = 2;
     struct Raw { uint4 w; };
-    static __device__ __forceinline__ Raw load_raw(const char* p) { return {ld_stream(p)}; }
-    static __device__ __forceinline__ void store_raw(char* p, const Raw& r) { st_stream(p, r.w); }
+    static __device__ __forceinline__ Raw load_raw(const char* p) { return {ld16(p)}; }
+    static __device__ __forceinline__ void store_raw(char* p, const Raw& r) { st16(p, r.w); }
     static __device__ __forceinline__ void unpack(const Raw& r, float x[8])
     {
         x[0] = bf16_lo(r.w.x); x[1] = bf16_hi(r.w.x);
@@ -67,39 +109,32 @@ struct Group<1> {
         r.w.w = pack_bf16x2(x[6], x[7]);
         return r;
     }
-    static __device__ __forceinline__ float round(float x) { return round_bf16(x); }
+    static __device__ __forceinline__ void round8(float x[8])
+    {
+#pragma unroll
+        for (int q = 0; q < 8; q += 2) round_bf16x2(x[q], x[q + 1]);
+    }
 };
 
 template <>
 struct Group<0> {
     static constexpr int kBytes = 4;
-    struct Raw { uint4 a, b; };
-    static __device__ __forceinline__ Raw load_raw(const char* p)
-    {
-        return {ld_stream(p), ld_stream(p + 16)};
-    }
-    static __device__ __forceinline__ void store_raw(char* p, const Raw& r)
-    {
-        st_stream(p, r.a);
-        st_stream(p + 16, r.b);
-    }
+    using Raw = U8;
+    static __device__ __forceinline__ Raw load_raw(const char* p) { return ld32(p); }
+    static __device__ __forceinline__ void store_raw(char* p, const Raw& r) { st32(p, r); }
     static __device__ __forceinline__ void unpack(const Raw& r, float x[8])
     {
-        x[0] = __uint_as_float(r.a.x); x[1] = __uint_as_float(r.a.y);
-        x[2] = __uint_as_float(r.a.z); x[3] = __uint_as_float(r.a.w);
-        x[4] = __uint_as_float(r.b.x); x[5] = __uint_as_float(r.b.y);
-        x[6] = __uint_as_float(r.b.z); x[7] = __uint_as_float(r.b.w);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = __uint_as_float(r.x[q]);
     }
     static __device__ __forceinline__ Raw pack(const float x[8])
     {
         Raw r;
-        r.a = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
-                         __float_as_uint(x[2]), __float_as_uint(x[3]));
-        r.b = make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]),
-                         __float_as_uint(x[6]), __float_as_uint(x[7]));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) r.x[q] = __float_as_uint(x[q]);
         return r;
     }
-    static __device__ __forceinline__ float round(float x) { return x; }
+    static __device__ __forceinline__ void round8(float[8]) {}
 };
 
 template <int DT>
@@ -116,8 +151,38 @@ __device__ __forceinline__ void store_group(char* p, const float x[8])
 
 // ------------------------------------------------------------ the ring fold
 
-// Sum of one 8-element group over the N slabs in ring order for chunk c:
-//   acc = x[c+1];  acc = R(acc + x[c+j]) for j = 2..N   (ranks mod N)
+// Sources of chunk c in ring order: src[j] = slab (c + 1 + j) mod N.
+template <int NT>
+__device__ __forceinline__ void ring_sources(const char* grads, int64_t slab, int c,
+                                             const char* src[NT])
+{
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        int r = c + 1 + j;            // <= 2N - 1: one wrap
+        if (r >= NT) r -= NT;
+        src[j] = grads + (int64_t)r * slab;
+    }
+}
+
+// Sum of one group over the NT slabs whose raw words are already loaded,
+// in ring order:  acc = x[0];  acc = R(acc + x[j]) for j = 1..NT-1.
+template <int GDT, int NT>
+__device__ __forceinline__ void fold_loaded(const typename Group<GDT>::Raw raw[NT], float acc[8])
+{
+    using G = Group<GDT>;
+    G::unpack(raw[0], acc);
+#pragma unroll
+    for (int j = 1; j < NT; ++j) {
+        float x[8];
+        G::unpack(raw[j], x);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], x[q]);
+        G::round8(acc);
+    }
+}
+
+// The same fold for a run-time N (any N up to 64): for chunk c,
+//   acc = x[c+1];  acc = R(acc + x[c+j]) for j = 2..N   (ranks mod N).
 // slab: bytes per slab; off: byte offset of the group inside a slab.
 // Loads are issued in batches so that several slabs are in flight at once.
 template <int GDT>
@@ -145,7 +210,8 @@ __device__ __forceinline__ void ring_fold(const char* __restrict__ grads, int64_
                 float x[8];
                 G::unpack(raw[k], x);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) acc[q] = G::round(__fadd_rn(acc[q], x[q]));
+                for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], x[q]);
+                G::round8(acc);
             }
         }
     }
@@ -157,10 +223,9 @@ template <int GDT>
 __device__ __forceinline__ void average8(float acc[8], const Avg& avg)
 {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        float y = avg.pow2 ? __fmul_rn(acc[q], avg.invN) : __fdiv_rn(acc[q], avg.fN);
-        acc[q] = Group<GDT>::round(y);
-    }
+    for (int q = 0; q < 8; ++q)
+        acc[q] = avg.pow2 ? __fmul_rn(acc[q], avg.invN) : __fdiv_rn(acc[q], avg.fN);
+    Group<GDT>::round8(acc);
 }
 
 // Sum of squares of 8 values, fp32, fixed pairwise order.
@@ -192,6 +257,16 @@ __device__ __forceinline__ void adamw_elem(float& theta, float& m, float& v, flo
 }
 
 // ------------------------------------------------------------ reductions
+
+// Sum over the 32 lanes of a warp in a fixed tree, fp32; lane 0 holds the
+// result.  Used for the 256-element norm segments: with the 8-element sums
+// below, each segment is a fixed 8-level pairwise fp32 tree.
+__device__ __forceinline__ float warp_sum_f32(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_down_sync(0xffffffffu, v, o));
+    return v;
+}
 
 // Sum over the 32 lanes of a warp in a fixed tree; lane 0 holds the result.
 __device__ __forceinline__ double warp_sum(double v)

@@ -89,8 +89,9 @@ cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 const char* last_kernel_name();
 void set_last_kernel_name(const char* name);
 
-// Blocks for a grid-stride kernel: one resident wave (SMs x resident blocks
-// per SM), fewer when `threads_needed` is smaller, at most `cap` if cap > 0.
-int grid_for(const void* kernel, int64_t threads_needed, int cap);
+// Blocks for a grid-stride kernel: `waves` resident waves (SMs x resident
+// blocks per SM; more than one lets blocks that finish early be replaced),
+// fewer when `threads_needed` is smaller, at most `cap` if cap > 0.
+int grid_for(const void* kernel, int64_t threads_needed, int cap, int waves);
 
 }  // namespace dpz

@@ -57,10 +57,10 @@ int blocks_per_sm(const void* fn)
 
 }  // namespace
 
-// One resident wave (SMs x blocks per SM), fewer if the chunk is short.
-int grid_for(const void* fn, int64_t threads_needed, int cap)
+// `waves` resident waves (SMs x blocks per SM), fewer if the chunk is short.
+int grid_for(const void* fn, int64_t threads_needed, int cap, int waves)
 {
-    int64_t g = (int64_t)device_sms() * blocks_per_sm(fn);
+    int64_t g = (int64_t)device_sms() * blocks_per_sm(fn) * (waves < 1 ? 1 : waves);
     int64_t need = (threads_needed + kBlock - 1) / kBlock;
     if (need < g) g = need;
     if (cap > 0 && g > cap) g = cap;
@@ -80,15 +80,27 @@ void set_last_kernel_name(const char* n) { g_last_kernel = n; }
 // of squares of its 256 averaged elements (fixed shuffle tree) into the slot
 // of that segment, so the partials do not depend on the grid.
 
+// Segments a warp takes per iteration: two when the loaded words of both fit
+// comfortably in registers (more bytes in flight per thread), else one.
+template <int GDT, int NT>
+struct SegsPerIter {
+    static constexpr int kRegsPerSlab = GDT == 1 ? 4 : 8;
+    static constexpr int value = (NT > 0 && NT * kRegsPerSlab <= 32) ? 2 : 1;
+};
+
 // Ring-order reduce + average of every chunk.  ALL = false: chunk c goes to
 // slab c only (reduce-scatter).  ALL = true: to every slab (all-reduce).
-// SUMSQ: per-segment sums of squares of the averages.
-template <int GDT, bool ALL, bool SUMSQ>
+// SUMSQ: per-segment sums of squares of the averages.  NT > 0: N == NT known
+// at compile time; NT == 0: any N, read from n_rt.
+template <int GDT, int NT, bool ALL, bool SUMSQ>
 __global__ void __launch_bounds__(kBlock)
-k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int N, Avg avg,
+k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
          WsHeader* __restrict__ hdr, double* __restrict__ partials)
 {
-    constexpr int ES = Group<GDT>::kBytes;
+    using G = Group<GDT>;
+    constexpr int ES = G::kBytes;
+    constexpr int U = SegsPerIter<GDT, NT>::value;
+    const int N = NT > 0 ? NT : n_rt;
     const int64_t slab = P * ES;
     const int64_t groups = C / kGroup;
     const int64_t segs = segments_per_chunk(C);
@@ -97,25 +109,52 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int N, Avg avg,
     const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
     if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     for (int c = 0; c < N; ++c) {
-        for (int64_t wb = first; wb < groups; wb += stride) {
-            const int64_t gi = wb + lane;
-            float ss = 0.0f;
-            if (gi < groups) {
-                const int64_t off = (c * C + gi * kGroup) * ES;
-                float acc[8];
-                ring_fold<GDT>(grads, slab, off, c, N, acc);
-                average8<GDT>(acc, avg);
-                if (SUMSQ) ss = sumsq8(acc);
-                const typename Group<GDT>::Raw out = Group<GDT>::pack(acc);
-                if (ALL) {
-                    for (int r = 0; r < N; ++r) Group<GDT>::store_raw(grads + r * slab + off, out);
-                } else {
-                    Group<GDT>::store_raw(grads + c * slab + off, out);
+        constexpr int NS = NT > 0 ? NT : 1;
+        const char* src[NS];
+        if constexpr (NT > 0) ring_sources<NT>(grads, slab, c, src);
+        for (int64_t wb0 = first * U; wb0 < groups; wb0 += stride * U) {
+            typename G::Raw raw[U][NS];
+            if constexpr (NT > 0) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t gi = wb0 + 32 * u + lane;
+                    if (gi < groups) {
+                        const int64_t off = (c * C + gi * kGroup) * ES;
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) raw[u][j] = G::load_raw(src[j] + off);
+                    }
                 }
             }
-            if (SUMSQ) {
-                const double t = warp_sum((double)ss);
-                if (lane == 0) partials[c * segs + wb / 32] = t;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t wb = wb0 + 32 * u;
+                const int64_t gi = wb + lane;
+                float ss = 0.0f;
+                if (gi < groups) {
+                    const int64_t off = (c * C + gi * kGroup) * ES;
+                    float acc[8];
+                    if constexpr (NT > 0)
+                        fold_loaded<GDT, NT>(raw[u], acc);
+                    else
+                        ring_fold<GDT>(grads, slab, off, c, N, acc);
+                    average8<GDT>(acc, avg);
+                    if (SUMSQ) ss = sumsq8(acc);
+                    const typename G::Raw out = G::pack(acc);
+                    if (ALL) {
+                        if constexpr (NT > 0) {
+#pragma unroll
+                            for (int j = 0; j < NT; ++j) G::store_raw(const_cast<char*>(src[j]) + off, out);
+                        } else {
+                            for (int r = 0; r < N; ++r) G::store_raw(grads + r * slab + off, out);
+                        }
+                    } else {
+                        G::store_raw(grads + c * slab + off, out);
+                    }
+                }
+                if (SUMSQ && wb < groups) {
+                    const float t = warp_sum_f32(ss);
+                    if (lane == 0) partials[c * segs + wb / 32] = (double)t;
+                }
             }
         }
     }
@@ -144,8 +183,8 @@ k_norm_owned(const char* __restrict__ grads, int64_t P, int64_t C, int N,
                 load_group<GDT>(grads + c * slab + (c * C + gi * kGroup) * ES, x);
                 ss = sumsq8(x);
             }
-            const double t = warp_sum((double)ss);
-            if (lane == 0) partials[c * segs + wb / 32] = t;
+            const float t = warp_sum_f32(ss);
+            if (lane == 0) partials[c * segs + wb / 32] = (double)t;
         }
     }
 }
@@ -211,15 +250,28 @@ k_allgather(char* __restrict__ w, int64_t P, int64_t C, int N)
 
 // ------------------------------------------------------------------ launchers
 
-template <int GDT, bool ALL, bool SUMSQ>
+template <int GDT, int NT, bool ALL, bool SUMSQ>
 static cudaError_t reduce_t(const Arena& a, const Avg& avg, void* grads, void* ws, cudaStream_t s)
 {
-    auto fn = k_reduce<GDT, ALL, SUMSQ>;
-    const int grid = grid_for((const void*)fn, a.C / kGroup, 0);
+    auto fn = k_reduce<GDT, NT, ALL, SUMSQ>;
+    constexpr int U = SegsPerIter<GDT, NT>::value;
+    const int grid = grid_for((const void*)fn, (a.C / kGroup + U - 1) / U, 0, 2);
     set_last_kernel_name(ALL ? "dpz_allreduce_avg" : SUMSQ ? "dpz_rs_avg_sumsq" : "dpz_rs_avg");
     fn<<<grid, kBlock, 0, s>>>(static_cast<char*>(grads), a.P, a.C, a.N, avg,
                                static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr);
     return cudaGetLastError();
+}
+
+template <int GDT, bool ALL, bool SUMSQ>
+static cudaError_t reduce_n(const Arena& a, const Avg& avg, void* grads, void* ws, cudaStream_t s)
+{
+    switch (a.N) {
+    case 1: return reduce_t<GDT, 1, ALL, SUMSQ>(a, avg, grads, ws, s);
+    case 2: return reduce_t<GDT, 2, ALL, SUMSQ>(a, avg, grads, ws, s);
+    case 4: return reduce_t<GDT, 4, ALL, SUMSQ>(a, avg, grads, ws, s);
+    case 8: return reduce_t<GDT, 8, ALL, SUMSQ>(a, avg, grads, ws, s);
+    default: return reduce_t<GDT, 0, ALL, SUMSQ>(a, avg, grads, ws, s);
+    }
 }
 
 cudaError_t launch_reduce(const Arena& a, const Avg& avg, void* grads, bool all_slabs, void* ws,
@@ -227,13 +279,13 @@ cudaError_t launch_reduce(const Arena& a, const Avg& avg, void* grads, bool all_
 {
     const bool sumsq = ws != nullptr && !all_slabs;
     if (a.gdt == 1) {
-        if (all_slabs) return reduce_t<1, true, false>(a, avg, grads, ws, s);
-        return sumsq ? reduce_t<1, false, true>(a, avg, grads, ws, s)
-                     : reduce_t<1, false, false>(a, avg, grads, ws, s);
+        if (all_slabs) return reduce_n<1, true, false>(a, avg, grads, ws, s);
+        return sumsq ? reduce_n<1, false, true>(a, avg, grads, ws, s)
+                     : reduce_n<1, false, false>(a, avg, grads, ws, s);
     }
-    if (all_slabs) return reduce_t<0, true, false>(a, avg, grads, ws, s);
-    return sumsq ? reduce_t<0, false, true>(a, avg, grads, ws, s)
-                 : reduce_t<0, false, false>(a, avg, grads, ws, s);
+    if (all_slabs) return reduce_n<0, true, false>(a, avg, grads, ws, s);
+    return sumsq ? reduce_n<0, false, true>(a, avg, grads, ws, s)
+                 : reduce_n<0, false, false>(a, avg, grads, ws, s);
 }
 
 cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaStream_t s)
@@ -242,10 +294,10 @@ cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaS
     const char* g = static_cast<const char*>(grads);
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     if (a.gdt == 1) {
-        const int grid = grid_for((const void*)k_norm_owned<1>, a.C / kGroup, 0);
+        const int grid = grid_for((const void*)k_norm_owned<1>, a.C / kGroup, 0, 2);
         k_norm_owned<1><<<grid, kBlock, 0, s>>>(g, a.P, a.C, a.N, hdr, ws_partials(ws));
     } else {
-        const int grid = grid_for((const void*)k_norm_owned<0>, a.C / kGroup, 0);
+        const int grid = grid_for((const void*)k_norm_owned<0>, a.C / kGroup, 0, 2);
         k_norm_owned<0><<<grid, kBlock, 0, s>>>(g, a.P, a.C, a.N, hdr, ws_partials(ws));
     }
     return cudaGetLastError();
@@ -269,10 +321,10 @@ cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s)
     set_last_kernel_name("dpz_allgather");
     char* w = static_cast<char*>(weights);
     if (a.wdt == 1) {
-        const int grid = grid_for((const void*)k_allgather<1>, a.C / kGroup, 0);
+        const int grid = grid_for((const void*)k_allgather<1>, a.C / kGroup, 0, 2);
         k_allgather<1><<<grid, kBlock, 0, s>>>(w, a.P, a.C, a.N);
     } else {
-        const int grid = grid_for((const void*)k_allgather<0>, a.C / kGroup, 0);
+        const int grid = grid_for((const void*)k_allgather<0>, a.C / kGroup, 0, 2);
         k_allgather<0><<<grid, kBlock, 0, s>>>(w, a.P, a.C, a.N);
     }
     return cudaGetLastError();

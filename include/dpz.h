@@ -33,13 +33,15 @@
  * (Lab 09 §2; A4 Part 3, ncclAvg).  The fold order never depends on the
  * launch configuration, so results are bit-for-bit reproducible.
  *
- * Alignment: every base pointer 16-byte aligned, and C*(element bytes) a
- * multiple of 16 (P % (8N) == 0 guarantees it for both dtypes).
+ * Alignment: bf16 buffers 16-byte aligned, fp32 buffers (master, m, v and
+ * fp32 gradients or weights) 32-byte aligned, the workspace 16-byte aligned;
+ * P % (8N) == 0, so that every chunk is a whole number of 8-element groups
+ * (each lane moves 8 elements with one 128- or 256-bit access).
  *
  * Status: every call returns DPZ_OK or an error code without launching
  * anything when an argument is invalid (null pointer, N out of range,
  * P <= 0, P % N != 0, bad dtype, step < 1, overlapping buffers), and
- * DPZ_ERR_ALIGN for misaligned pointers or chunks.  A CUDA launch failure
+ * DPZ_ERR_ALIGN for misaligned pointers or chunks (P/N not a multiple of 8).  A CUDA launch failure
  * returns DPZ_ERR_CUDA.  dpz_last_error() gives the calling thread's last
  * message.  NaN and Inf inputs are not special-cased: they propagate.
  *
@@ -129,9 +131,9 @@ DPZ_API int dp_allreduce_avg(void* grads, int64_t P, int N, int gdtype,
  * slab c, as left by dp_reduce_scatter_avg): each rank's sum of squares of its
  * shard, then the sum over ranks ("Distributed training", Gates: ZeRO stages
  * differ from DDP only in the order the global norm is summed).  Squares are
- * summed in fp32 over groups of 8 and in fp64 beyond, in an order fixed by P
- * and N alone (one partial per 256-element segment), so every entry point and
- * every launch configuration gives the same bits.
+ * summed in fp32 within each 256-element segment (a fixed pairwise tree) and
+ * in fp64 over segments, in an order fixed by P and N alone, so every entry
+ * point and every launch configuration gives the same bits.
  * Writes the norm into ws (for zero1_adamw_step) and, if norm_out is not
  * NULL, to *norm_out (device pointer to one float). */
 DPZ_API int dp_grad_global_norm(const void* grads, int64_t P, int N, int gdtype,

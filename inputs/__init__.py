@@ -173,7 +173,11 @@ SWEEP_SIZES = [4096 * 4 ** k for k in range(10)]   # 4 KiB .. 1 GiB
 ALLREDUCE_7B = Workload("allreduce-bf16-7b-n4", N=4, P=7_000_000_000, gdtype="bf16",
                         wdtype="bf16", grad=Dist(NORMAL, 1e-3), allreduce_only=True)
 
-WORKLOADS = {w.name: w for w in (TINY, GPT2_124M, GPT2_1P5B, ALLREDUCE_7B)}
+# The 1.5B workload's distributions on a 100M-parameter arena (2.8 GB resident,
+# still far larger than L2): the case profiler captures run on.
+PROFILE_1P5B_SHAPE = GPT2_1P5B.with_(name="zero1-n4-p100m-profile", P=100_000_000)
+
+WORKLOADS = {w.name: w for w in (TINY, GPT2_124M, GPT2_1P5B, ALLREDUCE_7B, PROFILE_1P5B_SHAPE)}
 
 
 # ---------------------------------------------------------------- host fill

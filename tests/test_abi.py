@@ -79,6 +79,9 @@ def _step(dpz, grads=A, master=A + 64 * MB, m=A + 80 * MB, v=A + 96 * MB,
     (dict(P=4 * 1028), 2),              # chunk 1028 not a multiple of 8
     (dict(grads=A + 8), 2),             # misaligned
     (dict(m=A + 80 * MB + 4), 2),
+    (dict(master=A + 64 * MB + 16), 2),  # fp32 buffers need 32-byte alignment
+    (dict(g=0, grads=A + 16), 2),        # fp32 gradients too
+    (dict(w=0, weights=A + 112 * MB + 16), 2),
     (dict(g=2), 1),                     # unknown dtype
     (dict(w=-1), 1),
     (dict(m=A + 64 * MB + 8192), 1),    # m overlaps master

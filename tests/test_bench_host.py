@@ -1,0 +1,78 @@
+"""bench.py's host logic without a GPU: the algorithmic byte counts, the
+max-over-ranks timing on a world-size-2 gloo group, and the reference arm's
+JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+import bench
+import inputs as I
+from conftest import ROOT
+
+
+def test_step_bytes_match_the_survey_table():
+    # N*P*e_g + 24*P + N*P*e_w: 40P for N = 4 bf16, 56P for N = 8 bf16
+    assert bench.step_bytes(I.GPT2_1P5B) == 40 * 1_557_611_200 == 62_304_448_000
+    assert bench.step_bytes(I.GPT2_124M) == 56 * 124_439_808
+    assert bench.step_bytes(I.TINY) == 4 * 4096 * 4 + 24 * 4096 + 4 * 4096 * 2 == 196_608
+    assert bench.step_bytes(I.ALLREDUCE_7B) == 2 * 4 * 7_000_000_000 * 2
+    # with clipping, the three kernels move 44P for the 1.5B workload
+    w = I.GPT2_1P5B
+    k = sum(bench.kernel_bytes(n, w) for n in ("dpz_rs_avg_sumsq", "dpz_adamw_bcast"))
+    assert k == 44 * w.P
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    m = bench.max_over_ranks(1.5 + rank, world)
+    bench.barrier(world)
+    q.put((rank, m))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    for p in ps:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got == {0: 2.5, 1: 2.5}
+
+
+def test_reference_arm_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", I.TINY.name, "--steps", "2", "--warmup", "0",
+                          "--ref-seconds", "0.2"], capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["metric"] == bench.METRIC
+
+
+def test_reference_arm_nonzero_rank_does_nothing():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", I.TINY.name, "--steps", "1", "--warmup", "0"],
+                         capture_output=True, text=True, timeout=120, env=env)
+    assert out.returncode == 0 and out.stdout.strip() == ""
