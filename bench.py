@@ -99,7 +99,7 @@ def ncu_traffic(kernel: str, w: I.Workload):
     if t.get("kernel_source_hash") != kernel_source_hash():
         return None
     k = t.get("kernels", {}).get(kernel)
-    if not k or k.get("N") != w.N:
+    if not k or (k.get("N"), k.get("gdtype"), k.get("wdtype")) != (w.N, w.gdtype, w.wdtype):
         return None
     return int(k["dram_bytes_per_element"] * w.P)
 
