@@ -332,6 +332,32 @@ DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v, void* 
     return ok();
 }
 
+DPZ_API int dp_grad_global_norm_static(const void* grads, int64_t P, int N, int gdtype,
+                                       float* norm_out, void* stream)
+{
+    DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_dtype(gdtype, "gradient"));
+    DPZ_TRY(check_ptr(grads, "grads", gdtype));
+    if (norm_out == nullptr) return fail(DPZ_ERR_INVALID_ARG, "norm_out is NULL");
+    const size_t need = ws_bytes_for(P, N);
+    if (need > static_scratch_bytes())
+        return fail(DPZ_ERR_INVALID_ARG,
+                    "N = %d slabs of P = %lld elements need %zu bytes of norm scratch, more than "
+                    "the %zu-byte static scratch; use dp_grad_global_norm with a workspace",
+                    N, (long long)P, need, static_scratch_bytes());
+    DPZ_TRY(check_disjoint({range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
+                            range("norm_out", norm_out, 4)}));
+    void* ws = nullptr;
+    const cudaError_t e = static_scratch_address(&ws);
+    if (e != cudaSuccess)
+        return fail(DPZ_ERR_CUDA, "address of the static norm scratch: %s", cudaGetErrorString(e));
+    const Arena a = make_arena(P, N, gdtype, gdtype);
+    cudaStream_t s = as_stream(stream);
+    DPZ_TRY(launch(s, [&] { return launch_norm_owned(a, grads, ws, s); }));
+    DPZ_TRY(launch(s, [&] { return launch_norm_finalize(a, ws, norm_out, s); }));
+    return ok();
+}
+
 DPZ_API int dpz_profile_start(int max_launches)
 {
     if (max_launches < 1 || max_launches > (1 << 20))

@@ -85,6 +85,12 @@ cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, Adam
                          float* v, void* weights, void* ws, cudaStream_t s);
 cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 
+// The fixed device scratch of dp_grad_global_norm_static (norm_static.cu):
+// its size in bytes, and its device address on the current device (looked
+// up on the first call on each device).
+size_t static_scratch_bytes();
+cudaError_t static_scratch_address(void** ptr);
+
 // Name of the kernel the last launcher call on this thread launched.
 const char* last_kernel_name();
 void set_last_kernel_name(const char* name);

@@ -52,6 +52,8 @@ _SIGS = {
     "dp_allgather": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _VP], ctypes.c_int),
     "dp_zero1_step": ([_VP, _FP, _FP, _FP, _VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                        ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _FP, _VP], ctypes.c_int),
+    "dp_grad_global_norm_static": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _FP, _VP],
+                                   ctypes.c_int),
     "dpz_last_error": ([], ctypes.c_char_p),
     "dpz_version": ([], ctypes.c_char_p),
     "dpz_launch_count": ([], ctypes.c_int64),
@@ -149,6 +151,12 @@ def dp_allreduce_avg(grads, N: int, stream=None) -> None:
 def dp_grad_global_norm(grads, N: int, ws, norm_out=None, stream=None) -> None:
     _check(lib.dp_grad_global_norm(_ptr(grads), _np(grads, N), N, dtype_code(grads), _ptr(ws),
                                    _ptr(norm_out), _stream_handle(stream)))
+
+
+def dp_grad_global_norm_static(grads, N: int, norm_out, stream=None) -> None:
+    """The global norm without a caller workspace (fixed device scratch)."""
+    _check(lib.dp_grad_global_norm_static(_ptr(grads), _np(grads, N), N, dtype_code(grads),
+                                          _ptr(norm_out), _stream_handle(stream)))
 
 
 def zero1_adamw_step(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None,

@@ -171,6 +171,28 @@ DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v,
                           int wdtype, const dpz_adamw_cfg* cfg, void* ws,
                           float* norm_out, void* stream);
 
+/* The global norm of dp_grad_global_norm for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this call.  It serves code
+ * that must not call cudaMalloc or any allocator of its own: a plug-in running
+ * inside a host framework whose caching allocator owns all device memory, or
+ * a service that reserves its whole memory budget up front.  Such a caller
+ * cannot provide the workspace of dp_grad_global_norm.  Here the partial sums
+ * live in a fixed 4 MiB array of device memory that the library declares at
+ * file scope, so the call allocates nothing; it needs
+ * dpz_workspace_bytes(P, N) <= 4 MiB (for example the GPT-2 124M arena at
+ * N = 8) and returns DPZ_ERR_INVALID_ARG with a clear message beyond that.
+ * Inputs and output are as in dp_grad_global_norm; norm_out (one float of
+ * device memory) is required.
+ *
+ * The first call on a device looks up the array's address on that device
+ * (cudaGetSymbolAddress), so make that first call before any stream capture.
+ * Every GPU that loads the library holds the 4 MiB array until the process
+ * exits.  All calls share it: each call clears what must start at zero, but
+ * calls whose kernels overlap on the GPU (unordered streams) race with each
+ * other and give wrong results. */
+DPZ_API int dp_grad_global_norm_static(const void* grads, int64_t P, int N,
+                                       int gdtype, float* norm_out, void* stream);
+
 /* The calling thread's last error message ("" if none). */
 DPZ_API const char* dpz_last_error(void);
 
