@@ -262,8 +262,9 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
-def config_of(w: I.Workload) -> dict:
-    c = {"workload": w.name, "ranks_simulated": w.N, "P": w.P, "grad_dtype": w.gdtype,
+def config_of(w: I.Workload, acc32: bool = False) -> dict:
+    c = {"workload": w.name, "ranks_simulated": w.N, "P": w.P,
+         "grad_dtype": w.gdtype + ("+fp32-accumulate" if acc32 else ""),
          "weight_dtype": w.wdtype, "state_dtype": "f32" if not w.allreduce_only else None,
          "clip": w.clip, "step_t": w.step,
          "l2": "inputs larger than L2 (resident arena %.1f GB vs 129 MB L2)" % (
@@ -308,9 +309,10 @@ def run_gpu(args) -> None:
 
     def step():
         if w.allreduce_only:
-            dpz.dp_allreduce_avg(G, w.N, stream)
+            dpz.dp_allreduce_avg(G, w.N, stream, acc32=args.acc32)
         else:
-            dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=stream)
+            dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=stream,
+                              acc32=args.acc32)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -369,7 +371,7 @@ def run_gpu(args) -> None:
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_max, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": config_of(w),
+            "data": "synthetic", "config": config_of(w, args.acc32),
             "steps_per_s": round(1e3 / ms_max, 3),
             "pct_of_hbm_roofline": {
                 "measured_copy_peak": round(100 * value / world / pk["hbm_gbs"], 2),
@@ -431,6 +433,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["dpz", "reference"], default="dpz")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--acc32", action="store_true",
+                    help="bf16 gradients reduced with fp32 accumulation (DPZ_BF16_ACC32)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

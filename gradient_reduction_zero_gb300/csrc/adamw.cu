@@ -164,6 +164,20 @@ cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, Adam
                          bool bcast, bool store_avg, void* grads, float* master, float* m,
                          float* v, void* weights, void* ws, cudaStream_t s)
 {
+    if (a.gdt == 2) {
+        // fp32-accumulating bf16 ring: only the fold differs; stored averages
+        // are plain bf16
+        if (src == AdamSrc::kFold) {
+            if (a.wdt == 1)
+                return adamw_dt<2, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
+                                      weights, ws, s);
+            return adamw_dt<2, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights,
+                                  ws, s);
+        }
+        Arena b = a;
+        b.gdt = 1;
+        return launch_adamw(b, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws, s);
+    }
     if (a.gdt == 1 && a.wdt == 1)
         return adamw_dt<1, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws,
                               s);

@@ -40,7 +40,7 @@ int ok()
     return DPZ_OK;
 }
 
-int elem_bytes(int dt) { return dt == DPZ_BF16 ? 2 : 4; }
+int elem_bytes(int dt) { return dt == DPZ_F32 ? 4 : 2; }
 
 // ------------------------------------------------------------ validation
 
@@ -63,10 +63,11 @@ int check_dims(int64_t P, int N)
     return DPZ_OK;
 }
 
-int check_dtype(int dt, const char* what)
+// Gradients: DPZ_F32, DPZ_BF16 or DPZ_BF16_ACC32; weights: DPZ_F32 or DPZ_BF16.
+int check_dtype(int dt, const char* what, bool gradient)
 {
-    if (dt != DPZ_F32 && dt != DPZ_BF16)
-        return fail(DPZ_ERR_INVALID_ARG, "%s dtype %d is neither DPZ_F32 nor DPZ_BF16", what, dt);
+    if (dt != DPZ_F32 && dt != DPZ_BF16 && !(gradient && dt == DPZ_BF16_ACC32))
+        return fail(DPZ_ERR_INVALID_ARG, "%s dtype %d is not supported", what, dt);
     return DPZ_OK;
 }
 
@@ -205,7 +206,7 @@ DPZ_API int64_t dpz_launch_count(void) { return g_launches.load(); }
 DPZ_API int dp_reduce_scatter_avg(void* grads, int64_t P, int N, int gdtype, void* stream)
 {
     DPZ_TRY(check_dims(P, N));
-    DPZ_TRY(check_dtype(gdtype, "gradient"));
+    DPZ_TRY(check_dtype(gdtype, "gradient", true));
     DPZ_TRY(check_ptr(grads, "grads", gdtype));
     const Arena a = make_arena(P, N, gdtype, gdtype);
     const Avg avg = make_avg(N);
@@ -218,7 +219,7 @@ DPZ_API int dp_reduce_scatter_avg(void* grads, int64_t P, int N, int gdtype, voi
 DPZ_API int dp_allreduce_avg(void* grads, int64_t P, int N, int gdtype, void* stream)
 {
     DPZ_TRY(check_dims(P, N));
-    DPZ_TRY(check_dtype(gdtype, "gradient"));
+    DPZ_TRY(check_dtype(gdtype, "gradient", true));
     DPZ_TRY(check_ptr(grads, "grads", gdtype));
     const Arena a = make_arena(P, N, gdtype, gdtype);
     const Avg avg = make_avg(N);
@@ -232,7 +233,7 @@ DPZ_API int dp_grad_global_norm(const void* grads, int64_t P, int N, int gdtype,
                                 float* norm_out, void* stream)
 {
     DPZ_TRY(check_dims(P, N));
-    DPZ_TRY(check_dtype(gdtype, "gradient"));
+    DPZ_TRY(check_dtype(gdtype, "gradient", true));
     DPZ_TRY(check_ptr(grads, "grads", gdtype));
     DPZ_TRY(check_ptr(ws, "ws"));
     std::vector<Range> rs = {range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
@@ -252,8 +253,8 @@ static int check_step_buffers(const void* grads, const float* master, const floa
                               const float* norm_out)
 {
     DPZ_TRY(check_dims(P, N));
-    DPZ_TRY(check_dtype(gdtype, "gradient"));
-    DPZ_TRY(check_dtype(wdtype, "weight"));
+    DPZ_TRY(check_dtype(gdtype, "gradient", true));
+    DPZ_TRY(check_dtype(wdtype, "weight", false));
     DPZ_TRY(check_cfg(cfg));
     DPZ_TRY(check_ptr(grads, "grads", gdtype));
     DPZ_TRY(check_ptr(master, "master", DPZ_F32));
@@ -292,7 +293,7 @@ DPZ_API int zero1_adamw_step(const void* grads, float* master, float* m, float* 
 DPZ_API int dp_allgather(void* weights, int64_t P, int N, int wdtype, void* stream)
 {
     DPZ_TRY(check_dims(P, N));
-    DPZ_TRY(check_dtype(wdtype, "weight"));
+    DPZ_TRY(check_dtype(wdtype, "weight", false));
     DPZ_TRY(check_ptr(weights, "weights", wdtype));
     const Arena a = make_arena(P, N, wdtype, wdtype);
     cudaStream_t s = as_stream(stream);
@@ -336,7 +337,7 @@ DPZ_API int dp_grad_global_norm_static(const void* grads, int64_t P, int N, int 
                                        float* norm_out, void* stream)
 {
     DPZ_TRY(check_dims(P, N));
-    DPZ_TRY(check_dtype(gdtype, "gradient"));
+    DPZ_TRY(check_dtype(gdtype, "gradient", true));
     DPZ_TRY(check_ptr(grads, "grads", gdtype));
     if (norm_out == nullptr) return fail(DPZ_ERR_INVALID_ARG, "norm_out is NULL");
     const size_t need = ws_bytes_for(P, N);

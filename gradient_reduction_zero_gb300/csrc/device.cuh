@@ -83,7 +83,10 @@ __device__ __forceinline__ void round_bf16x2(float& lo, float& hi)
 }
 
 // A group of 8 elements of one storage type.  DT 0 = fp32 (one 32-byte
-// word), DT 1 = bf16 (one 16-byte word).
+// word), DT 1 = bf16 (one 16-byte word), DT 2 = bf16 storage whose ring
+// accumulates in fp32.  round8 is the rounding to the storage type;
+// hop_round8 the rounding after each ring hop (a bf16 ring rounds once per
+// hop; the fp32-accumulating one only at the end).
 template <int DT>
 struct Group;
 
@@ -114,6 +117,12 @@ struct Group<1> {
 #pragma unroll
         for (int q = 0; q < 8; q += 2) round_bf16x2(x[q], x[q + 1]);
     }
+    static __device__ __forceinline__ void hop_round8(float x[8]) { round8(x); }
+};
+
+template <>
+struct Group<2> : Group<1> {
+    static __device__ __forceinline__ void hop_round8(float[8]) {}
 };
 
 template <>
@@ -135,6 +144,7 @@ struct Group<0> {
         return r;
     }
     static __device__ __forceinline__ void round8(float[8]) {}
+    static __device__ __forceinline__ void hop_round8(float[8]) {}
 };
 
 template <int DT>
@@ -177,7 +187,7 @@ __device__ __forceinline__ void fold_loaded(const typename Group<GDT>::Raw raw[N
         G::unpack(raw[j], x);
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], x[q]);
-        G::round8(acc);
+        G::hop_round8(acc);
     }
 }
 
@@ -211,7 +221,7 @@ __device__ __forceinline__ void ring_fold(const char* __restrict__ grads, int64_
                 G::unpack(raw[k], x);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], x[q]);
-                G::round8(acc);
+                G::hop_round8(acc);
             }
         }
     }

@@ -84,7 +84,7 @@ void set_last_kernel_name(const char* n) { g_last_kernel = n; }
 // comfortably in registers (more bytes in flight per thread), else one.
 template <int GDT, int NT>
 struct SegsPerIter {
-    static constexpr int kRegsPerSlab = GDT == 1 ? 4 : 8;
+    static constexpr int kRegsPerSlab = GDT == 0 ? 8 : 4;
     static constexpr int value = (NT > 0 && NT * kRegsPerSlab <= 32) ? 2 : 1;
 };
 
@@ -278,6 +278,11 @@ cudaError_t launch_reduce(const Arena& a, const Avg& avg, void* grads, bool all_
                           cudaStream_t s)
 {
     const bool sumsq = ws != nullptr && !all_slabs;
+    if (a.gdt == 2) {
+        if (all_slabs) return reduce_n<2, true, false>(a, avg, grads, ws, s);
+        return sumsq ? reduce_n<2, false, true>(a, avg, grads, ws, s)
+                     : reduce_n<2, false, false>(a, avg, grads, ws, s);
+    }
     if (a.gdt == 1) {
         if (all_slabs) return reduce_n<1, true, false>(a, avg, grads, ws, s);
         return sumsq ? reduce_n<1, false, true>(a, avg, grads, ws, s)
@@ -293,7 +298,7 @@ cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaS
     set_last_kernel_name("dpz_norm_owned");
     const char* g = static_cast<const char*>(grads);
     WsHeader* hdr = static_cast<WsHeader*>(ws);
-    if (a.gdt == 1) {
+    if (a.gdt != 0) {      // both bf16 modes store bf16 averages
         const int grid = grid_for((const void*)k_norm_owned<1>, a.C / kGroup, 0, 2);
         k_norm_owned<1><<<grid, kBlock, 0, s>>>(g, a.P, a.C, a.N, hdr, ws_partials(ws));
     } else {

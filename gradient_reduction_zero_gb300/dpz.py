@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdpz.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "dpz.h")
 
-F32, BF16 = 0, 1
+F32, BF16, BF16_ACC32 = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_ALIGN, ERR_CUDA = 0, 1, 2, 3
 MAX_RANKS = 64
 
@@ -97,10 +97,14 @@ def _torch():
     return torch
 
 
-def dtype_code(t) -> int:
+def dtype_code(t, acc32: bool = False) -> int:
+    """DPZ dtype code of a tensor; acc32 selects the fp32-accumulating ring for
+    a bf16 gradient arena."""
     torch = _torch()
     if t.dtype == torch.bfloat16:
-        return BF16
+        return BF16_ACC32 if acc32 else BF16
+    if acc32:
+        raise TypeError("fp32 accumulation applies to bf16 gradient arenas")
     if t.dtype == torch.float32:
         return F32
     raise TypeError(f"unsupported dtype {t.dtype}")
@@ -138,13 +142,13 @@ def _np(arena, N: int) -> int:
 
 # ------------------------------------------------------------ the calls
 
-def dp_reduce_scatter_avg(grads, N: int, stream=None) -> None:
-    _check(lib.dp_reduce_scatter_avg(_ptr(grads), _np(grads, N), N, dtype_code(grads),
+def dp_reduce_scatter_avg(grads, N: int, stream=None, acc32: bool = False) -> None:
+    _check(lib.dp_reduce_scatter_avg(_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32),
                                      _stream_handle(stream)))
 
 
-def dp_allreduce_avg(grads, N: int, stream=None) -> None:
-    _check(lib.dp_allreduce_avg(_ptr(grads), _np(grads, N), N, dtype_code(grads),
+def dp_allreduce_avg(grads, N: int, stream=None, acc32: bool = False) -> None:
+    _check(lib.dp_allreduce_avg(_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32),
                                 _stream_handle(stream)))
 
 
@@ -172,9 +176,9 @@ def dp_allgather(weights, N: int, stream=None) -> None:
 
 
 def dp_zero1_step(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None, norm_out=None,
-                  stream=None) -> None:
+                  stream=None, acc32: bool = False) -> None:
     _check(lib.dp_zero1_step(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
-                             _np(grads, N), N, dtype_code(grads), dtype_code(weights),
+                             _np(grads, N), N, dtype_code(grads, acc32), dtype_code(weights),
                              ctypes.byref(cfg), _ptr(ws), _ptr(norm_out),
                              _stream_handle(stream)))
 

@@ -68,6 +68,15 @@ extern "C" {
 /* element types */
 #define DPZ_F32 0
 #define DPZ_BF16 1
+/* Gradients only: bf16 storage whose ring accumulates in fp32 (13.5 Multi-GPU
+ * from First Principles, Exercise 8, second variant: each rank's vector is
+ * rounded to bf16 once and the sum is accumulated in fp32).  The fold is
+ *     acc = x[(c+1)%N][i];  acc = acc + x[(c+j)%N][i]  (fp32, j = 2..N)
+ * and the stored average is RNE_bf16(acc / N), one rounding in all.  The
+ * arena, the stored averages and every byte moved are those of DPZ_BF16; in
+ * a ring of processes the partial sums would travel as fp32 (twice the
+ * reduce-scatter's bytes), here they stay in registers. */
+#define DPZ_BF16_ACC32 2
 
 /* status codes */
 #define DPZ_OK 0

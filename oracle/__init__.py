@@ -16,7 +16,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "liboracle.so")
 
-F32, BF16, F64 = 0, 1, 2
+F32, BF16, F64, BF16_ACC32 = 0, 1, 2, 3
 
 
 def build() -> str:
@@ -59,6 +59,8 @@ def lib():
             "orc_average_owned": ([_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                    ctypes.c_int], ctypes.c_int),
             "orc_ring_allreduce_avg": ([_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                        ctypes.c_int, _P], ctypes.c_int),
+            "orc_reduce_scatter_avg": ([_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
                                         ctypes.c_int, _P], ctypes.c_int),
             "orc_star_allreduce": ([_P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, _P],
                                    ctypes.c_int),
@@ -124,12 +126,22 @@ def bf16_to_f32(h) -> np.ndarray:
     return (h.astype(np.uint32) << 16).view(np.float32)
 
 
-def ring_reduce_scatter(arena: np.ndarray, rho: int = 1, steps: int | None = None):
-    """In place on arena[N][P]; returns bytes sent per rank."""
+def _code(arena: np.ndarray, acc32: bool) -> int:
+    if acc32:
+        if arena.dtype != np.uint16:
+            raise TypeError("fp32 accumulation applies to bf16 arenas")
+        return BF16_ACC32
+    return dtype_code(arena)
+
+
+def ring_reduce_scatter(arena: np.ndarray, rho: int = 1, steps: int | None = None,
+                        acc32: bool = False):
+    """In place on arena[N][P]; returns bytes sent per rank.  acc32: a bf16
+    arena whose ring carries fp32 partial sums."""
     N, P = arena.shape
     steps = N - 1 if steps is None else steps
     sent = np.zeros(N, dtype=np.int64)
-    _chk(lib().orc_ring_reduce_scatter(_ptr(arena), N, P, dtype_code(arena), rho, steps,
+    _chk(lib().orc_ring_reduce_scatter(_ptr(arena), N, P, _code(arena, acc32), rho, steps,
                                        _ptr(sent)), "reduce-scatter")
     return sent
 
@@ -152,10 +164,21 @@ def average_owned(arena: np.ndarray, rho: int = 1) -> None:
     _chk(lib().orc_average_owned(_ptr(arena), N, P, dtype_code(arena), rho), "average")
 
 
-def ring_allreduce_avg(arena: np.ndarray, rho: int = 1):
+def reduce_scatter_avg(arena: np.ndarray, rho: int = 1, acc32: bool = False):
+    """Reduce-scatter then owner average in one ring session (needed for acc32,
+    whose fp32 partial sums exist only inside the ring).  In place; only the
+    owner chunks are meaningful afterwards.  Returns bytes sent per rank."""
     N, P = arena.shape
     sent = np.zeros(N, dtype=np.int64)
-    _chk(lib().orc_ring_allreduce_avg(_ptr(arena), N, P, dtype_code(arena), rho,
+    _chk(lib().orc_reduce_scatter_avg(_ptr(arena), N, P, _code(arena, acc32), rho, _ptr(sent)),
+         "reduce-scatter")
+    return sent
+
+
+def ring_allreduce_avg(arena: np.ndarray, rho: int = 1, acc32: bool = False):
+    N, P = arena.shape
+    sent = np.zeros(N, dtype=np.int64)
+    _chk(lib().orc_ring_allreduce_avg(_ptr(arena), N, P, _code(arena, acc32), rho,
                                       _ptr(sent)), "all-reduce")
     return sent
 
@@ -194,7 +217,8 @@ def adamw(theta, m, v, grad, cfg: AdamWCfg, scale: float = 1.0) -> None:
                     ctypes.byref(cfg), scale)
 
 
-def zero1_step(grads, master, m, v, weights, cfg: AdamWCfg, ext_sumsq: float = -1.0):
+def zero1_step(grads, master, m, v, weights, cfg: AdamWCfg, ext_sumsq: float = -1.0,
+               acc32: bool = False):
     """In place.  Returns (norm, scale, sent_rs, sent_ag)."""
     N, P = grads.shape
     assert weights.shape == (N, P)
@@ -203,7 +227,7 @@ def zero1_step(grads, master, m, v, weights, cfg: AdamWCfg, ext_sumsq: float = -
     srs = np.zeros(N, dtype=np.int64)
     sag = np.zeros(N, dtype=np.int64)
     _chk(lib().orc_zero1_step(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
-                              N, P, dtype_code(grads), dtype_code(weights), ctypes.byref(cfg),
+                              N, P, _code(grads, acc32), dtype_code(weights), ctypes.byref(cfg),
                               ext_sumsq, ctypes.addressof(norm), ctypes.addressof(scale),
                               _ptr(srs), _ptr(sag)), "zero1 step")
     return norm.value, scale.value, srs, sag

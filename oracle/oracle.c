@@ -21,9 +21,16 @@ static size_t elem_bytes(int dt)
     return dt == ORC_F64 ? 8u : dt == ORC_F32 ? 4u : 2u;
 }
 
+/* bytes of one element in a rank's working buffer and in a reduce-scatter
+ * message: the fp32-accumulating bf16 ring works in fp32 */
+static size_t work_bytes(int dt)
+{
+    return dt == ORC_BF16_ACC32 ? 4u : elem_bytes(dt);
+}
+
 static int valid_dtype(int dt)
 {
-    return dt == ORC_F32 || dt == ORC_BF16 || dt == ORC_F64;
+    return dt == ORC_F32 || dt == ORC_BF16 || dt == ORC_F64 || dt == ORC_BF16_ACC32;
 }
 
 uint16_t orc_f32_to_bf16(float x)
@@ -60,7 +67,7 @@ static void add_into(int dt, void* local, const void* msg, int64_t n)
         double* a = (double*)local;
         const double* b = (const double*)msg;
         for (int64_t i = 0; i < n; ++i) a[i] = a[i] + b[i];
-    } else if (dt == ORC_F32) {
+    } else if (dt == ORC_F32 || dt == ORC_BF16_ACC32) {
         float* a = (float*)local;
         const float* b = (const float*)msg;
         for (int64_t i = 0; i < n; ++i) a[i] = a[i] + b[i];
@@ -77,7 +84,7 @@ static void add_into(int dt, void* local, const void* msg, int64_t n)
 static double load_as_double(int dt, const void* p, int64_t i)
 {
     if (dt == ORC_F64) return ((const double*)p)[i];
-    if (dt == ORC_F32) return (double)((const float*)p)[i];
+    if (dt == ORC_F32 || dt == ORC_BF16_ACC32) return (double)((const float*)p)[i];
     return (double)orc_bf16_to_f32(((const uint16_t*)p)[i]);
 }
 
@@ -95,7 +102,7 @@ typedef struct {
     int N;
     int64_t P, C;
     int dt;
-    size_t es;
+    size_t es;              /* bytes per element in the working buffers */
     unsigned char** rank;   /* rank[r] = rank r's own full buffer */
     unsigned char** msg;    /* msg[r]  = the chunk rank r sends this step */
 } ring_t;
@@ -107,7 +114,7 @@ static int ring_open(ring_t* R, const void* arena, int N, int64_t P, int dt)
     R->P = P;
     R->C = P / N;
     R->dt = dt;
-    R->es = elem_bytes(dt);
+    R->es = work_bytes(dt);
     R->rank = (unsigned char**)calloc((size_t)N, sizeof(void*));
     R->msg = (unsigned char**)calloc((size_t)N, sizeof(void*));
     if (!R->rank || !R->msg) return -1;
@@ -115,8 +122,14 @@ static int ring_open(ring_t* R, const void* arena, int N, int64_t P, int dt)
         R->rank[r] = (unsigned char*)malloc((size_t)P * R->es);
         R->msg[r] = (unsigned char*)malloc((size_t)R->C * R->es);
         if (!R->rank[r] || !R->msg[r]) return -1;
-        memcpy(R->rank[r], (const unsigned char*)arena + (size_t)r * P * R->es,
-               (size_t)P * R->es);
+        if (dt == ORC_BF16_ACC32) {
+            const uint16_t* src = (const uint16_t*)arena + (size_t)r * P;
+            float* dst = (float*)R->rank[r];
+            for (int64_t i = 0; i < P; ++i) dst[i] = orc_bf16_to_f32(src[i]);
+        } else {
+            memcpy(R->rank[r], (const unsigned char*)arena + (size_t)r * P * R->es,
+                   (size_t)P * R->es);
+        }
     }
     return 0;
 }
@@ -124,9 +137,15 @@ static int ring_open(ring_t* R, const void* arena, int N, int64_t P, int dt)
 static void ring_close(ring_t* R, void* arena)
 {
     for (int r = 0; r < R->N; ++r) {
-        if (arena && R->rank[r])
+        if (arena && R->rank[r] && R->dt == ORC_BF16_ACC32) {
+            /* working fp32 values back to bf16 storage */
+            uint16_t* dst = (uint16_t*)arena + (size_t)r * R->P;
+            const float* src = (const float*)R->rank[r];
+            for (int64_t i = 0; i < R->P; ++i) dst[i] = orc_f32_to_bf16(src[i]);
+        } else if (arena && R->rank[r]) {
             memcpy((unsigned char*)arena + (size_t)r * R->P * R->es, R->rank[r],
                    (size_t)R->P * R->es);
+        }
         free(R->rank[r]);
         free(R->msg[r]);
     }
@@ -171,11 +190,14 @@ static void ag_steps(ring_t* R, int rho, int steps, int64_t* sent)
     const int N = R->N;
     int64_t* ch = (int64_t*)malloc((size_t)N * sizeof(int64_t));
     const size_t bytes = (size_t)R->C * R->es;
+    /* what a message carries on the wire: the storage type (the averages of
+     * the fp32-accumulating bf16 ring are bf16 values) */
+    const size_t wire = (size_t)R->C * elem_bytes(R->dt);
     for (int t = 0; t < steps; ++t) {
         for (int r = 0; r < N; ++r) {
             ch[r] = pmod((int64_t)r + 1 - rho - t, N);
             memcpy(R->msg[r], chunk_ptr(R, r, ch[r]), bytes);
-            if (sent) sent[r] += (int64_t)bytes;
+            if (sent) sent[r] += (int64_t)wire;
         }
         for (int r = 0; r < N; ++r) {
             int dst = (r + 1) % N;
@@ -197,6 +219,9 @@ static void average_owned_ring(ring_t* R, int rho)
             } else if (R->dt == ORC_F32) {
                 float* a = (float*)p;
                 a[i] = a[i] / (float)N;
+            } else if (R->dt == ORC_BF16_ACC32) {
+                float* a = (float*)p;
+                a[i] = orc_bf16_to_f32(orc_f32_to_bf16(a[i] / (float)N));
             } else {
                 uint16_t* a = (uint16_t*)p;
                 a[i] = orc_f32_to_bf16(orc_bf16_to_f32(a[i]) / (float)N);
@@ -229,6 +254,17 @@ int orc_average_owned(void* arena, int N, int64_t P, int dtype, int rho)
 {
     ring_t R;
     if (ring_open(&R, arena, N, P, dtype)) return -1;
+    average_owned_ring(&R, rho);
+    ring_close(&R, arena);
+    return 0;
+}
+
+int orc_reduce_scatter_avg(void* arena, int N, int64_t P, int dtype, int rho,
+                           int64_t* sent)
+{
+    ring_t R;
+    if (ring_open(&R, arena, N, P, dtype)) return -1;
+    rs_steps(&R, rho, N - 1, sent);
     average_owned_ring(&R, rho);
     ring_close(&R, arena);
     return 0;
@@ -359,6 +395,9 @@ int orc_zero1_step(void* grads, float* master, float* m, float* v,
     ring_t G;
     if (ring_open(&G, grads, N, P, gdtype)) return -1;
     const int64_t C = G.C;
+    /* AdamW reads the averaged chunk from the working buffer: fp32 words for
+     * the fp32-accumulating ring (bf16 values after the owner's rounding) */
+    const int gwork = gdtype == ORC_BF16_ACC32 ? ORC_F32 : gdtype;
 
     /* 1. reduce-scatter, 2. the owner averages its chunk */
     rs_steps(&G, rho, N - 1, sent_rs);
@@ -381,7 +420,7 @@ int orc_zero1_step(void* grads, float* master, float* m, float* v,
         memcpy(sh_t, master + off, (size_t)C * 4u);
         memcpy(sh_m, m + off, (size_t)C * 4u);
         memcpy(sh_v, v + off, (size_t)C * 4u);
-        orc_adamw(sh_t, sh_m, sh_v, chunk_ptr(&G, r, r), gdtype, C, cfg, scale);
+        orc_adamw(sh_t, sh_m, sh_v, chunk_ptr(&G, r, r), gwork, C, cfg, scale);
         cast_weights(sh_t, chunk_ptr(&W, r, r), wdtype, C);
         memcpy(master + off, sh_t, (size_t)C * 4u);
         memcpy(m + off, sh_m, (size_t)C * 4u);
@@ -436,7 +475,8 @@ int orc_zero0_step(void* grads, float* master_full, float* m_full,
         float* th = master_full + (size_t)r * P;
         float* mm = m_full + (size_t)r * P;
         float* vv = v_full + (size_t)r * P;
-        orc_adamw(th, mm, vv, G.rank[r], gdtype, P, cfg, scale);
+        orc_adamw(th, mm, vv, G.rank[r], gdtype == ORC_BF16_ACC32 ? ORC_F32 : gdtype, P, cfg,
+                  scale);
         cast_weights(th, (unsigned char*)weights + (size_t)r * P * elem_bytes(wdtype),
                      wdtype, P);
     }

@@ -29,7 +29,14 @@
 extern "C" {
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2, ORC_BF16_ACC32 = 3 };
+
+/* ORC_BF16_ACC32: bf16 storage whose ring carries fp32 partial sums ("13.5
+ * Multi-GPU from First Principles", Exercise 8, second variant: each vector
+ * is rounded to bf16 once and the sum is accumulated in fp32).  The rank
+ * buffers hold the bf16 values as floats, reduce-scatter messages are fp32
+ * (4 bytes per element), the owner's average is rounded to bf16 once, and
+ * all-gather messages carry those bf16 averages (2 bytes per element). */
 
 typedef struct {
     float lr, beta1, beta2, eps, weight_decay;
@@ -62,6 +69,11 @@ int orc_owner(int c, int N, int rho);
 /* The owner of every chunk divides its fully reduced chunk by N (sum, then
  * divide), rounding to the storage type. */
 int orc_average_owned(void* arena, int N, int64_t P, int dtype, int rho);
+
+/* Reduce-scatter then owner average in one ring session (the partial sums of
+ * the fp32-accumulating bf16 ring exist only inside the ring). */
+int orc_reduce_scatter_avg(void* arena, int N, int64_t P, int dtype, int rho,
+                           int64_t* sent);
 
 /* Full ring all-reduce-average: reduce-scatter, owner average, all-gather. */
 int orc_ring_allreduce_avg(void* arena, int N, int64_t P, int dtype, int rho,

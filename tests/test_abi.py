@@ -82,7 +82,8 @@ def _step(dpz, grads=A, master=A + 64 * MB, m=A + 80 * MB, v=A + 96 * MB,
     (dict(master=A + 64 * MB + 16), 2),  # fp32 buffers need 32-byte alignment
     (dict(g=0, grads=A + 16), 2),        # fp32 gradients too
     (dict(w=0, weights=A + 112 * MB + 16), 2),
-    (dict(g=2), 1),                     # unknown dtype
+    (dict(g=3), 1),                     # unknown dtype
+    (dict(w=2), 1),                     # fp32 accumulation is a gradient mode only
     (dict(w=-1), 1),
     (dict(m=A + 64 * MB + 8192), 1),    # m overlaps master
     (dict(weights=A + 32 * 1024), 1),   # weights overlap grads (4*4096*4 bytes)

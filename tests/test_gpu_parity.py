@@ -103,16 +103,17 @@ def make_problem(N, C, gdt, wdt, clip, seed, step=1000, gsigma=1e-3):
     return w, g, th, m, v, wts
 
 
-def run_gpu_step(w, g, th, m, v, wts, store_avg=True, want_norm=True, fused=True):
+def run_gpu_step(w, g, th, m, v, wts, store_avg=True, want_norm=True, fused=True, acc32=False):
     G, T, M, V, W = up(g), up(th), up(m), up(v), up(wts)
     ws = dpz.workspace(w.P, w.N, DEV)
     nrm = torch.full((1,), -1.0, device=DEV)
     cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip,
                        store_avg=store_avg)
     if fused:
-        dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm if want_norm else None)
+        dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm if want_norm else None,
+                          acc32=acc32)
     else:
-        dpz.dp_reduce_scatter_avg(G, w.N)
+        dpz.dp_reduce_scatter_avg(G, w.N, acc32=acc32)
         if w.clip > 0 or want_norm:
             dpz.dp_grad_global_norm(G, w.N, ws, nrm)
         dpz.zero1_adamw_step(G, T, M, V, W, w.N, cfg, ws=ws)
@@ -121,11 +122,11 @@ def run_gpu_step(w, g, th, m, v, wts, store_avg=True, want_norm=True, fused=True
     return down(G), down(T), down(M), down(V), down(W), nrm.item()
 
 
-def check_step(w, g, th, m, v, wts, out, check_avg=True):
+def check_step(w, g, th, m, v, wts, out, check_avg=True, acc32=False):
     Gg, Tg, Mg, Vg, Wg, gnorm = out
     cfg = O.cfg_from_workload(w)
     G, T, M, V, W = g.copy(), th.copy(), m.copy(), v.copy(), wts.copy()
-    onorm, oscale, _, _ = O.zero1_step(G, T, M, V, W, cfg)
+    onorm, oscale, _, _ = O.zero1_step(G, T, M, V, W, cfg, acc32=acc32)
     C = w.C
     if gnorm >= 0:
         assert abs(gnorm - onorm) <= 1e-6 * onorm, (gnorm, onorm)
@@ -303,3 +304,49 @@ def test_profiling_and_launch_count():
     assert dpz.launch_count() - before == 3
     assert set(stats) == {"dpz_rs_avg_sumsq", "dpz_norm_finalize", "dpz_adamw_bcast"}
     assert all(n == 1 and ms > 0 for n, ms in stats.values())
+
+
+# ----------------------------------------------------------- fp32-accumulating bf16 ring
+
+@pytest.mark.parametrize("N,C", SHAPES)
+def test_acc32_reduce_scatter(N, C):
+    g = rand_grads(N, C, "bf16", seed=5 * N + 1)
+    ref = g.copy()
+    O.reduce_scatter_avg(ref, acc32=True)
+    G = up(g)
+    dpz.dp_reduce_scatter_avg(G, N, acc32=True)
+    out = down(G)
+    for c in range(N):
+        sl = slice(c * C, (c + 1) * C)
+        for r in range(N):
+            want = ref[c, sl] if r == c else g[r, sl]
+            assert same_bits(out[r, sl], want), (r, c)
+
+
+@pytest.mark.parametrize("N,C", [(1, 8), (2, 2056), (3, 1000), (4, 6152), (8, 12344), (64, 72)])
+def test_acc32_allreduce(N, C):
+    g = rand_grads(N, C, "bf16", seed=9 + N)
+    ref = g.copy()
+    O.ring_allreduce_avg(ref, acc32=True)
+    G = up(g)
+    dpz.dp_allreduce_avg(G, N, acc32=True)
+    assert same_bits(down(G), ref)
+
+
+@pytest.mark.parametrize("N,C", [(1, 4104), (3, 1000), (4, 6152), (8, 12344), (16, 520)])
+@pytest.mark.parametrize("wdt", ["bf16", "f32"])
+@pytest.mark.parametrize("clip", [0.0, 1e-3])
+def test_acc32_zero1_step(N, C, wdt, clip):
+    w, g, th, m, v, wts = make_problem(N, C, "bf16", wdt, clip, seed=2 * N + 3)
+    out = run_gpu_step(w, g, th, m, v, wts, acc32=True)
+    check_step(w, g, th, m, v, wts, out, acc32=True)
+
+
+@pytest.mark.parametrize("clip", [0.0, 1e-3])
+def test_acc32_fused_equals_unfused(clip):
+    w, g, th, m, v, wts = make_problem(4, 6152, "bf16", "bf16", clip, seed=12)
+    a = run_gpu_step(w, g, th, m, v, wts, fused=True, acc32=True)
+    b = run_gpu_step(w, g, th, m, v, wts, fused=False, acc32=True)
+    for x, y in zip(a[:5], b[:5]):
+        assert same_bits(x, y)
+    assert a[5] == b[5]

@@ -492,3 +492,99 @@ def test_oracle_rejects_bad_arguments():
     grads, master, m, v, w = _rand_problem(2, 8, "f32", "f32", 1)
     with pytest.raises(ValueError):
         O.zero1_step(grads, master, m, v, w, _cfg(t=0))
+
+
+# ------------------------------------------- bf16 ring with fp32 accumulation
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 8])
+def test_acc32_integer_valued_is_exact(N):
+    """With every partial sum exact, both bf16 rings give the correctly
+    rounded exact mean."""
+    rng = np.random.default_rng(40 + N)
+    C = 16
+    vals = rng.integers(-16, 17, size=(N, N * C)).astype(np.float32)
+    a = O.f32_to_bf16(vals)
+    O.reduce_scatter_avg(a, acc32=True)
+    for c in range(N):
+        for i in range(C):
+            e = c * C + i
+            want = _exact_avg_f32(vals[:, e], N)
+            want_bf = torch.tensor([want]).to(torch.bfloat16).view(torch.int16).item() & 0xFFFF
+            assert int(a[c, e]) == want_bf
+
+
+@pytest.mark.parametrize("N", [2, 3, 5, 8, 64])
+def test_acc32_is_one_rounding_of_the_fp32_fold(N):
+    """13.5 Multi-GPU from First Principles, Exercise 8, second variant: the
+    inputs are bf16 once, the ring's sum is an fp32 left fold in ring order,
+    and the average is rounded to bf16 once."""
+    rng = np.random.default_rng(7 * N + 1)
+    C = 8
+    xb = O.f32_to_bf16(rng.standard_normal((N, N * C)).astype(np.float32))
+    xf = O.bf16_to_f32(xb)
+    a = xb.copy()
+    O.reduce_scatter_avg(a, acc32=True)
+    for c in range(N):
+        sl = slice(c * C, (c + 1) * C)
+        acc = xf[(c + 1) % N, sl].copy()
+        for j in range(2, N + 1):
+            acc = (acc + xf[(c + j) % N, sl]).astype(np.float32)
+        avg = (acc / np.float32(N)).astype(np.float32)
+        want = torch.from_numpy(avg).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(a[c, sl], want)
+
+
+def test_acc32_differs_from_per_hop_rounding():
+    """256 + 1 + 1 in a bf16 ring: per-hop rounding loses both ones (257
+    rounds to 256), fp32 accumulation keeps them (258 / 3 = 86)."""
+    N = 3
+    x = np.zeros((N, N), dtype=np.float32)
+    # chunk 0 is folded in rank order 1, 2, 0
+    x[1, 0], x[2, 0], x[0, 0] = 256.0, 1.0, 1.0
+    xb = O.f32_to_bf16(x)
+    hop, acc = xb.copy(), xb.copy()
+    O.reduce_scatter_avg(hop)
+    O.reduce_scatter_avg(acc, acc32=True)
+    assert O.bf16_to_f32(hop[0, 0:1])[0] == np.float32(O.bf16_to_f32(O.f32_to_bf16(
+        np.array([256.0 / 3], dtype=np.float32)))[0])
+    assert O.bf16_to_f32(acc[0, 0:1])[0] == 86.0
+
+
+@pytest.mark.parametrize("N", [2, 4, 8])
+def test_acc32_bytes(N):
+    """fp32 partial sums double the reduce-scatter's message bytes; the
+    all-gather still moves bf16 averages."""
+    P = 8 * N * 4
+    a = np.zeros((N, P), dtype=np.uint16)
+    sent = O.reduce_scatter_avg(a.copy(), acc32=True)
+    assert np.all(sent == (N - 1) * P * 4 // N)
+    both = O.ring_allreduce_avg(a.copy(), acc32=True)
+    assert np.all(both == (N - 1) * P * 4 // N + (N - 1) * P * 2 // N)
+
+
+@pytest.mark.parametrize("clip", [0.0, 1e-3])
+@pytest.mark.parametrize("N", [1, 3, 4, 8])
+def test_acc32_zero1_equals_zero0(N, clip):
+    C = 24
+    grads, master, m, v, w = _rand_problem(N, C, "bf16", "bf16", 3 * N + int(clip > 0))
+    cfg = _cfg(1.5e-4, 0.9, 0.95, 1e-8, 0.1, 1000, clip)
+    g1, t1, m1, v1, w1 = grads.copy(), master.copy(), m.copy(), v.copy(), w.copy()
+    n1, _, _, _ = O.zero1_step(g1, t1, m1, v1, w1, cfg, acc32=True)
+    g0 = grads.copy()
+    t0, m0, v0 = (np.tile(x, (N, 1)) for x in (master, m, v))
+    w0 = w.copy()
+    N_, P_ = g0.shape
+    norm = __import__("ctypes").c_float()
+    sent = np.zeros(N, dtype=np.int64)
+    rc = O.lib().orc_zero0_step(g0.ctypes.data, t0.ctypes.data, m0.ctypes.data, v0.ctypes.data,
+                                w0.ctypes.data, N_, P_, O.BF16_ACC32, O.BF16,
+                                __import__("ctypes").byref(cfg),
+                                __import__("ctypes").addressof(norm), sent.ctypes.data)
+    assert rc == 0 and norm.value == n1
+    for r in range(N):
+        assert np.array_equal(t0[r], t1) and np.array_equal(w0[r], w1[r])
+    # the averages match the standalone reduce-scatter's
+    a = grads.copy()
+    O.reduce_scatter_avg(a, acc32=True)
+    for c in range(N):
+        assert np.array_equal(g1[c, c * C:(c + 1) * C], a[c, c * C:(c + 1) * C])
