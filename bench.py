@@ -307,11 +307,12 @@ def run_gpu(args) -> None:
     cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step(on=None):
+        on = stream if on is None else on
         if w.allreduce_only:
-            dpz.dp_allreduce_avg(G, w.N, stream, acc32=args.acc32)
+            dpz.dp_allreduce_avg(G, w.N, on, acc32=args.acc32)
         else:
-            dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=stream,
+            dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=on,
                               acc32=args.acc32)
 
     for _ in range(max(3, args.warmup)):
@@ -357,6 +358,11 @@ def run_gpu(args) -> None:
                   "share": round(t / sum(x[1] for x in kstats.values()), 4)}
               for k, (n, t) in kstats.items()}
 
+    # ---------------------------------------------------------------- graph
+    graph = None
+    if args.graph:
+        graph = run_graph(args, step, stream, world, nbytes)
+
     # ---------------------------------------------------------------- e2e
     e2e = None
     if not args.no_e2e:
@@ -390,10 +396,38 @@ def run_gpu(args) -> None:
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if graph is not None:
+            line["graph_replay"] = graph
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_graph(args, step, stream, world, nbytes):
+    """The same step captured once in a CUDA graph and replayed K times."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        step_on = torch.cuda.current_stream()
+        step(step_on)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    return {"ms_per_step": round(ms, 5), "steps_per_s": round(1e3 / ms, 1),
+            "value": round(nbytes * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT}
 
 
 def run_e2e(args, w, G, step, nrm, stream, world):
@@ -433,6 +467,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["dpz", "reference"], default="dpz")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured in a CUDA graph and replayed")
     ap.add_argument("--acc32", action="store_true",
                     help="bf16 gradients reduced with fp32 accumulation (DPZ_BF16_ACC32)")
     ap.add_argument("--no-e2e", action="store_true")

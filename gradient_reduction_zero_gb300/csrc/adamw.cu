@@ -39,8 +39,8 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
     const int64_t segs = segments_per_chunk(C);
     const int lane = threadIdx.x & 31;
     const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
-    if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
-    for (int c = 0; c < N; ++c) {
+    if (SUMSQ && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->arrive = 0u;
+    for (int c = blockIdx.y; c < N; c += gridDim.y) {
         constexpr int NS = NT > 0 ? NT : 1;
         const char* src[NS];
         if constexpr (NT > 0) ring_sources<NT>(grads, gslab, c, src);
@@ -108,7 +108,7 @@ static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bo
     auto fn = k_adamw<GDT, WDT, NT, FOLD, BCAST, SUMSQ>;
     // the load-owner kernel balances better with blocks that replace early
     // finishers; the fold kernel is register-heavier and keeps two waves
-    const int grid = grid_for((const void*)fn, a.C / kGroup, 0, FOLD ? 2 : 4);
+    const dim3 grid = grid_chunks((const void*)fn, a.C / kGroup, a.N, FOLD ? 2 : 4);
     set_last_kernel_name(FOLD ? (SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused")
                               : (BCAST ? "dpz_adamw_bcast" : "dpz_adamw_owner"));
     fn<<<grid, kBlock, 0, s>>>(static_cast<char*>(grads), master, m, v,

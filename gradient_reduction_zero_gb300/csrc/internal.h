@@ -100,4 +100,8 @@ void set_last_kernel_name(const char* name);
 // fewer when `threads_needed` is smaller, at most `cap` if cap > 0.
 int grid_for(const void* kernel, int64_t threads_needed, int cap, int waves);
 
+// Grid of a chunk-major streaming kernel: (blocks per chunk, N) when the N
+// chunks fit side by side in `waves` resident waves, else (wave, 1).
+dim3 grid_chunks(const void* kernel, int64_t threads_per_chunk, int N, int waves);
+
 }  // namespace dpz

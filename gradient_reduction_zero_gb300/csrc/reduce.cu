@@ -68,6 +68,19 @@ int grid_for(const void* fn, int64_t threads_needed, int cap, int waves)
     return (int)g;
 }
 
+// Grid of a chunk-major streaming kernel.  When the blocks that one chunk
+// needs, times N, fit in `waves` resident waves, every chunk gets its own
+// row of blocks (grid.y = N) and the chunks run side by side; otherwise a
+// single row walks the chunks in turn (grid.y = 1).
+dim3 grid_chunks(const void* fn, int64_t threads_per_chunk, int N, int waves)
+{
+    const int64_t wave = (int64_t)device_sms() * blocks_per_sm(fn) * (waves < 1 ? 1 : waves);
+    int64_t per_chunk = (threads_per_chunk + kBlock - 1) / kBlock;
+    if (per_chunk < 1) per_chunk = 1;
+    if (per_chunk * N <= wave) return dim3((unsigned)per_chunk, (unsigned)N, 1);
+    return dim3((unsigned)(per_chunk < wave ? per_chunk : wave), 1, 1);
+}
+
 const char* last_kernel_name() { return g_last_kernel; }
 void set_last_kernel_name(const char* n) { g_last_kernel = n; }
 
@@ -107,8 +120,8 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int lane = threadIdx.x & 31;
     const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
-    if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
-    for (int c = 0; c < N; ++c) {
+    if (SUMSQ && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->arrive = 0u;
+    for (int c = blockIdx.y; c < N; c += gridDim.y) {
         constexpr int NS = NT > 0 ? NT : 1;
         const char* src[NS];
         if constexpr (NT > 0) ring_sources<NT>(grads, slab, c, src);
@@ -173,8 +186,8 @@ k_norm_owned(const char* __restrict__ grads, int64_t P, int64_t C, int N,
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int lane = threadIdx.x & 31;
     const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
-    if (blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
-    for (int c = 0; c < N; ++c) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->arrive = 0u;
+    for (int c = blockIdx.y; c < N; c += gridDim.y) {
         for (int64_t wb = first; wb < groups; wb += stride) {
             const int64_t gi = wb + lane;
             float ss = 0.0f;
@@ -237,7 +250,7 @@ k_allgather(char* __restrict__ w, int64_t P, int64_t C, int N)
     const int64_t slab = P * ES;
     const int64_t groups = C / kGroup;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int c = 0; c < N; ++c) {
+    for (int c = blockIdx.y; c < N; c += gridDim.y) {
         for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups;
              gi += stride) {
             const int64_t off = (c * C + gi * kGroup) * ES;
@@ -255,7 +268,7 @@ static cudaError_t reduce_t(const Arena& a, const Avg& avg, void* grads, void* w
 {
     auto fn = k_reduce<GDT, NT, ALL, SUMSQ>;
     constexpr int U = SegsPerIter<GDT, NT>::value;
-    const int grid = grid_for((const void*)fn, (a.C / kGroup + U - 1) / U, 0, 2);
+    const dim3 grid = grid_chunks((const void*)fn, (a.C / kGroup + U - 1) / U, a.N, 2);
     set_last_kernel_name(ALL ? "dpz_allreduce_avg" : SUMSQ ? "dpz_rs_avg_sumsq" : "dpz_rs_avg");
     fn<<<grid, kBlock, 0, s>>>(static_cast<char*>(grads), a.P, a.C, a.N, avg,
                                static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr);
@@ -299,10 +312,10 @@ cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaS
     const char* g = static_cast<const char*>(grads);
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     if (a.gdt != 0) {      // both bf16 modes store bf16 averages
-        const int grid = grid_for((const void*)k_norm_owned<1>, a.C / kGroup, 0, 2);
+        const dim3 grid = grid_chunks((const void*)k_norm_owned<1>, a.C / kGroup, a.N, 2);
         k_norm_owned<1><<<grid, kBlock, 0, s>>>(g, a.P, a.C, a.N, hdr, ws_partials(ws));
     } else {
-        const int grid = grid_for((const void*)k_norm_owned<0>, a.C / kGroup, 0, 2);
+        const dim3 grid = grid_chunks((const void*)k_norm_owned<0>, a.C / kGroup, a.N, 2);
         k_norm_owned<0><<<grid, kBlock, 0, s>>>(g, a.P, a.C, a.N, hdr, ws_partials(ws));
     }
     return cudaGetLastError();
@@ -326,10 +339,10 @@ cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s)
     set_last_kernel_name("dpz_allgather");
     char* w = static_cast<char*>(weights);
     if (a.wdt == 1) {
-        const int grid = grid_for((const void*)k_allgather<1>, a.C / kGroup, 0, 2);
+        const dim3 grid = grid_chunks((const void*)k_allgather<1>, a.C / kGroup, a.N, 2);
         k_allgather<1><<<grid, kBlock, 0, s>>>(w, a.P, a.C, a.N);
     } else {
-        const int grid = grid_for((const void*)k_allgather<0>, a.C / kGroup, 0, 2);
+        const dim3 grid = grid_chunks((const void*)k_allgather<0>, a.C / kGroup, a.N, 2);
         k_allgather<0><<<grid, kBlock, 0, s>>>(w, a.P, a.C, a.N);
     }
     return cudaGetLastError();

@@ -48,6 +48,12 @@
  * Streams: the caller orders producers of `grads` before the call with
  * events (A4 Part 3: record an event on the compute stream, make the
  * communication stream wait on it), and consumers after it.
+ *
+ * CUDA graphs: dp_reduce_scatter_avg, dp_allreduce_avg, dp_grad_global_norm,
+ * zero1_adamw_step, dp_allgather and dp_zero1_step only enqueue kernels on
+ * `stream`, so they can be captured into a CUDA graph and replayed.  Call
+ * each once outside capture first (its launch configuration is cached per
+ * device) and keep profiling off while capturing.
  */
 #ifndef DPZ_H
 #define DPZ_H

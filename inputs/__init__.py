@@ -178,6 +178,8 @@ ALLREDUCE_7B = Workload("allreduce-bf16-7b-n4", N=4, P=7_000_000_000, gdtype="bf
 PROFILE_1P5B_SHAPE = GPT2_1P5B.with_(name="zero1-n4-p100m-profile", P=100_000_000)
 
 WORKLOADS = {w.name: w for w in (TINY, GPT2_124M, GPT2_1P5B, ALLREDUCE_7B, PROFILE_1P5B_SHAPE)}
+WORKLOADS.update({w.name: w for w in (allreduce_sweep(s, n) for s in SWEEP_SIZES
+                                      for n in (2, 4, 8))})
 
 
 # ---------------------------------------------------------------- host fill
