@@ -358,6 +358,11 @@ def run_gpu(args) -> None:
                   "share": round(t / sum(x[1] for x in kstats.values()), 4)}
               for k, (n, t) in kstats.items()}
 
+    # ---------------------------------------------------------------- buckets
+    bucketed = None
+    if args.buckets and not w.allreduce_only:
+        bucketed = run_buckets(args, w, G, T, M, V, W, ws, nrm, cfg, stream)
+
     # ---------------------------------------------------------------- graph
     graph = None
     if args.graph:
@@ -398,10 +403,89 @@ def run_gpu(args) -> None:
         }
         if graph is not None:
             line["graph_replay"] = graph
+        if bucketed is not None:
+            line["bucket_overlap"] = bucketed
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def segment_bounds(P: int, N: int, k: int):
+    """k buckets covering [0, P), bounds on 256-element segment boundaries of
+    their chunks, in backward (last-first) order."""
+    C = P // N
+    edges = [0]
+    for i in range(1, k):
+        b = P * i // k
+        c = b // C
+        edges.append(c * C + (b - c * C) // 256 * 256)
+    edges.append(P)
+    edges = sorted(set(edges))
+    return [(edges[i], edges[i + 1] - edges[i]) for i in range(len(edges) - 1)][::-1]
+
+
+def run_buckets(args, w, G, T, M, V, W, ws, nrm, cfg, stream):
+    """Overlap of the reduce-scatter with a simulated backward pass.  The
+    backward writes the gradient arena bucket by bucket (the seeded input
+    generator, last bucket first) on the main stream.  Serial: the whole
+    backward, then dp_zero1_step.  Overlapped: after each bucket an event;
+    a second stream waits on it and reduces that bucket
+    (dp_reduce_scatter_avg_range), then finalises the norm and runs
+    dp_zero1_update once the last bucket is in.  Both compute the same step."""
+    import torch
+    import gradient_reduction_zero_gb300.dpz as dpz
+    es = w.grad_bytes()
+    base = G.data_ptr()
+    buckets = segment_bounds(w.P, w.N, args.buckets)
+    main = stream
+    comm = torch.cuda.Stream()
+
+    def backward_bucket(lo, n):
+        for r in range(w.N):
+            I.dev_fill(base + (r * w.P + lo) * es, w.gdtype, lo, n, w.grad_seed + r,
+                       I.STREAM_GRAD, w.grad, main.cuda_stream)
+
+    def serial():
+        for lo, n in buckets:
+            backward_bucket(lo, n)
+        dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=main)
+
+    def overlapped():
+        comm.wait_stream(main)
+        for lo, n in buckets:
+            backward_bucket(lo, n)
+            ev = torch.cuda.Event()
+            ev.record(main)
+            comm.wait_event(ev)
+            dpz.dp_reduce_scatter_avg_range(G, w.N, lo, n, ws=ws, stream=comm)
+        dpz.dp_grad_norm_finalize(ws, w.P, w.N, nrm, stream=comm)
+        dpz.dp_zero1_update(G, T, M, V, W, w.N, cfg, ws=ws, stream=comm)
+        main.wait_stream(comm)
+
+    def backward_only():
+        for lo, n in buckets:
+            backward_bucket(lo, n)
+
+    def timed(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        for _ in range(reps):
+            fn()
+        e1.record(main)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    t_back = timed(backward_only)
+    t_serial = timed(serial)
+    t_over = timed(overlapped)
+    t_step = t_serial - t_back
+    return {"buckets": len(buckets), "backward_ms": round(t_back, 3),
+            "serial_ms": round(t_serial, 3), "overlapped_ms": round(t_over, 3),
+            "step_ms_in_serial": round(t_step, 3),
+            "step_hidden_fraction": round((t_serial - t_over) / t_step, 3) if t_step > 0 else None}
 
 
 def run_graph(args, step, stream, world, nbytes):
@@ -467,6 +551,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["dpz", "reference"], default="dpz")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--buckets", type=int, default=0,
+                    help="also measure a bucketed step overlapped with a simulated backward")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured in a CUDA graph and replayed")
     ap.add_argument("--acc32", action="store_true",

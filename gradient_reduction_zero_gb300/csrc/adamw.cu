@@ -10,12 +10,15 @@ namespace dpz {
 
 // NT > 0: N == NT known at compile time (the fold and the broadcast unroll);
 // NT == 0: any N, read from n_rt.
+// Without FOLD the average of element e (chunk c) is read at
+// grads + (c*avg_stride + e) elements: avg_stride = P for the owner slabs of
+// the arena, 0 for a compact [P] buffer of gradient shards.
 template <int GDT, int WDT, int NT, bool FOLD, bool BCAST, bool SUMSQ>
 __global__ void __launch_bounds__(kBlock)
 k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
         float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int n_rt,
         Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
-        double* __restrict__ partials)
+        double* __restrict__ partials, int64_t avg_stride)
 {
     const int N = NT > 0 ? NT : n_rt;
     constexpr int GES = Group<GDT>::kBytes;
@@ -64,7 +67,7 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
                     if (SUMSQ) ss = sumsq8(g);
                     if (store_avg) store_group<GDT>(grads + c * gslab + e * GES, g);
                 } else {
-                    load_group<GDT>(grads + c * gslab + e * GES, g);
+                    load_group<GDT>(grads + (c * avg_stride + e) * GES, g);
                 }
                 float th[8], mm[8], vv[8];
                 load_group<0>(reinterpret_cast<const char*>(master + e), th);
@@ -103,7 +106,7 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
 template <int GDT, int WDT, int NT, bool FOLD, bool BCAST, bool SUMSQ>
 static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
                            void* grads, float* master, float* m, float* v, void* weights,
-                           void* ws, cudaStream_t s)
+                           void* ws, cudaStream_t s, int64_t avg_stride)
 {
     auto fn = k_adamw<GDT, WDT, NT, FOLD, BCAST, SUMSQ>;
     // the load-owner kernel balances better with blocks that replace early
@@ -114,7 +117,7 @@ static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bo
     fn<<<grid, kBlock, 0, s>>>(static_cast<char*>(grads), master, m, v,
                                static_cast<char*>(weights), a.P, a.C, a.N, avg, h,
                                store_avg ? 1 : 0, static_cast<WsHeader*>(ws),
-                               SUMSQ ? ws_partials(ws) : nullptr);
+                               SUMSQ ? ws_partials(ws) : nullptr, avg_stride);
     return cudaGetLastError();
 }
 
@@ -126,43 +129,45 @@ static cudaError_t fused_n(const Arena& a, const Avg& avg, const AdamArgs& h, bo
     switch (a.N) {
     case 1:
         return adamw_t<GDT, WDT, 1, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s);
+                                                      weights, ws, s, a.P);
     case 2:
         return adamw_t<GDT, WDT, 2, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s);
+                                                      weights, ws, s, a.P);
     case 4:
         return adamw_t<GDT, WDT, 4, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s);
+                                                      weights, ws, s, a.P);
     case 8:
         return adamw_t<GDT, WDT, 8, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s);
+                                                      weights, ws, s, a.P);
     default:
         return adamw_t<GDT, WDT, 0, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s);
+                                                      weights, ws, s, a.P);
     }
 }
 
 template <int GDT, int WDT>
 static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                             bool bcast, bool store_avg, void* grads, float* master, float* m,
-                            float* v, void* weights, void* ws, cudaStream_t s)
+                            float* v, void* weights, void* ws, cudaStream_t s,
+                            int64_t avg_stride)
 {
     if (src == AdamSrc::kFold) {
         if (ws != nullptr)
             return fused_n<GDT, WDT, true>(a, avg, h, store_avg, grads, master, m, v, weights, ws,
                                            s);
-        return fused_n<GDT, WDT, false>(a, avg, h, store_avg, grads, master, m, v, weights, ws, s);
+        return fused_n<GDT, WDT, false>(a, avg, h, store_avg, grads, master, m, v, weights, ws,
+                                        s);
     }
     if (bcast)
         return adamw_t<GDT, WDT, 0, false, true, false>(a, avg, h, false, grads, master, m, v,
-                                                       weights, ws, s);
+                                                       weights, ws, s, avg_stride);
     return adamw_t<GDT, WDT, 0, false, false, false>(a, avg, h, false, grads, master, m, v,
-                                                    weights, ws, s);
+                                                    weights, ws, s, avg_stride);
 }
 
 cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                          bool bcast, bool store_avg, void* grads, float* master, float* m,
-                         float* v, void* weights, void* ws, cudaStream_t s)
+                         float* v, void* weights, void* ws, cudaStream_t s, int64_t avg_stride)
 {
     if (a.gdt == 2) {
         // fp32-accumulating bf16 ring: only the fold differs; stored averages
@@ -170,25 +175,26 @@ cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, Adam
         if (src == AdamSrc::kFold) {
             if (a.wdt == 1)
                 return adamw_dt<2, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                                      weights, ws, s);
-            return adamw_dt<2, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights,
-                                  ws, s);
+                                      weights, ws, s, avg_stride);
+            return adamw_dt<2, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
+                                  weights, ws, s, avg_stride);
         }
         Arena b = a;
         b.gdt = 1;
-        return launch_adamw(b, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws, s);
+        return launch_adamw(b, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws, s,
+                            avg_stride);
     }
     if (a.gdt == 1 && a.wdt == 1)
-        return adamw_dt<1, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws,
-                              s);
+        return adamw_dt<1, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
+                              weights, ws, s, avg_stride);
     if (a.gdt == 1 && a.wdt == 0)
-        return adamw_dt<1, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws,
-                              s);
+        return adamw_dt<1, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
+                              weights, ws, s, avg_stride);
     if (a.gdt == 0 && a.wdt == 1)
-        return adamw_dt<0, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws,
-                              s);
-    return adamw_dt<0, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws,
-                          s);
+        return adamw_dt<0, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
+                              weights, ws, s, avg_stride);
+    return adamw_dt<0, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
+                          weights, ws, s, avg_stride);
 }
 
 }  // namespace dpz

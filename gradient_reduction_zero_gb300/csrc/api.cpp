@@ -285,7 +285,7 @@ DPZ_API int zero1_adamw_step(const void* grads, float* master, float* m, float* 
     DPZ_TRY(launch(s, [&] {
         return launch_adamw(a, avg, h, AdamSrc::kLoadOwner, false, false,
                             const_cast<void*>(grads), master, m, v, weights,
-                            const_cast<void*>(ws), s);
+                            const_cast<void*>(ws), s, P);
     }));
     return ok();
 }
@@ -319,18 +319,145 @@ DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v, void* 
         DPZ_TRY(launch(s, [&] { return launch_norm_finalize(a, ws, norm_out, s); }));
         DPZ_TRY(launch(s, [&] {
             return launch_adamw(a, avg, h, AdamSrc::kLoadOwner, true, false, grads, master, m, v,
-                                weights, ws, s);
+                                weights, ws, s, P);
         }));
     } else {
         void* sws = norm_out ? ws : nullptr;
         DPZ_TRY(launch(s, [&] {
             return launch_adamw(a, avg, h, AdamSrc::kFold, true, cfg->store_avg != 0, grads,
-                                master, m, v, weights, sws, s);
+                                master, m, v, weights, sws, s, P);
         }));
         if (norm_out)
             DPZ_TRY(launch(s, [&] { return launch_norm_finalize(a, ws, norm_out, s); }));
     }
     return ok();
+}
+
+// ---------------------------------------------------------- buckets, ZeRO-2
+
+static int check_range(int64_t P, int N, int64_t lo, int64_t n, bool segment_aligned)
+{
+    if (lo < 0 || n <= 0 || lo > P - n)
+        return fail(DPZ_ERR_INVALID_ARG, "range [%lld, %lld) is not inside [0, %lld)",
+                    (long long)lo, (long long)(lo + n), (long long)P);
+    if (lo % kGroup != 0 || n % kGroup != 0)
+        return fail(DPZ_ERR_ALIGN, "range start %lld and length %lld must be multiples of 8",
+                    (long long)lo, (long long)n);
+    const int64_t C = P / N;
+    if (segment_aligned && (((lo % C) % kSegment) != 0 || (((lo + n) % C) % kSegment) != 0))
+        return fail(DPZ_ERR_ALIGN,
+                    "with norm partials the range [%lld, %lld) must start and end on "
+                    "256-element segment boundaries of its chunks (chunk = %lld)",
+                    (long long)lo, (long long)(lo + n), (long long)C);
+    return DPZ_OK;
+}
+
+DPZ_API int dp_reduce_scatter_avg_range(void* grads, int64_t P, int N, int gdtype, int64_t lo,
+                                        int64_t n, void* ws, void* stream)
+{
+    DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_dtype(gdtype, "gradient", true));
+    DPZ_TRY(check_ptr(grads, "grads", gdtype));
+    DPZ_TRY(check_range(P, N, lo, n, ws != nullptr));
+    if (ws) {
+        DPZ_TRY(check_ptr(ws, "ws"));
+        DPZ_TRY(check_disjoint({range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
+                                range("ws", ws, (int64_t)dpz_workspace_bytes(P, N))}));
+    }
+    const Arena a = make_arena(P, N, gdtype, gdtype);
+    const Avg avg = make_avg(N);
+    const int es = elem_bytes(gdtype);
+    const RangeArgs g{static_cast<char*>(grads) + lo * es, P, grads, P, lo, lo + n};
+    cudaStream_t s = as_stream(stream);
+    DPZ_TRY(launch(s, [&] { return launch_reduce_range(a, avg, g, ws, s); }));
+    return ok();
+}
+
+DPZ_API int dp_reduce_scatter_avg_bucket(const void* staging, int64_t lo, int64_t n, void* shards,
+                                         int64_t P, int N, int gdtype, void* ws, void* stream)
+{
+    DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_dtype(gdtype, "gradient", true));
+    DPZ_TRY(check_ptr(staging, "staging", gdtype));
+    DPZ_TRY(check_ptr(shards, "shards", gdtype));
+    DPZ_TRY(check_range(P, N, lo, n, ws != nullptr));
+    const int es = elem_bytes(gdtype);
+    std::vector<Range> rs = {range("staging", staging, int64_t(N) * n * es),
+                             range("shards", shards, P * es)};
+    if (ws) {
+        DPZ_TRY(check_ptr(ws, "ws"));
+        rs.push_back(range("ws", ws, (int64_t)dpz_workspace_bytes(P, N)));
+    }
+    DPZ_TRY(check_disjoint(rs));
+    const Arena a = make_arena(P, N, gdtype, gdtype);
+    const Avg avg = make_avg(N);
+    const RangeArgs g{staging, n, shards, 0, lo, lo + n};
+    cudaStream_t s = as_stream(stream);
+    DPZ_TRY(launch(s, [&] { return launch_reduce_range(a, avg, g, ws, s); }));
+    return ok();
+}
+
+DPZ_API int dp_grad_norm_finalize(void* ws, int64_t P, int N, float* norm_out, void* stream)
+{
+    DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_ptr(ws, "ws"));
+    if (norm_out)
+        DPZ_TRY(check_disjoint({range("ws", ws, (int64_t)dpz_workspace_bytes(P, N)),
+                                range("norm_out", norm_out, 4)}));
+    const Arena a = make_arena(P, N, DPZ_BF16, DPZ_BF16);
+    cudaStream_t s = as_stream(stream);
+    DPZ_TRY(launch(s, [&] { return launch_norm_finalize(a, ws, norm_out, s); }));
+    return ok();
+}
+
+static int update_common(const void* avg_src, int64_t avg_stride, int64_t avg_elems,
+                         float* master, float* m, float* v, void* weights, int64_t P, int N,
+                         int gdtype, int wdtype, const dpz_adamw_cfg* cfg, const void* ws,
+                         void* stream, const char* what)
+{
+    DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_dtype(gdtype, "gradient", true));
+    DPZ_TRY(check_dtype(wdtype, "weight", false));
+    DPZ_TRY(check_cfg(cfg));
+    DPZ_TRY(check_ptr(avg_src, what, gdtype));
+    DPZ_TRY(check_ptr(master, "master", DPZ_F32));
+    DPZ_TRY(check_ptr(m, "m", DPZ_F32));
+    DPZ_TRY(check_ptr(v, "v", DPZ_F32));
+    DPZ_TRY(check_ptr(weights, "weights", wdtype));
+    const bool clip = cfg->clip_norm > 0.0f;
+    if (clip) DPZ_TRY(check_ptr(ws, "ws"));
+    std::vector<Range> rs = {range(what, avg_src, avg_elems * elem_bytes(gdtype)),
+                             range("master", master, P * 4), range("m", m, P * 4),
+                             range("v", v, P * 4),
+                             range("weights", weights, int64_t(N) * P * elem_bytes(wdtype))};
+    if (ws) rs.push_back(range("ws", ws, (int64_t)dpz_workspace_bytes(P, N)));
+    DPZ_TRY(check_disjoint(rs));
+    const Arena a = make_arena(P, N, gdtype, wdtype);
+    const Avg avg = make_avg(N);
+    const AdamArgs h = make_adam(cfg);
+    cudaStream_t s = as_stream(stream);
+    DPZ_TRY(launch(s, [&] {
+        return launch_adamw(a, avg, h, AdamSrc::kLoadOwner, true, false,
+                            const_cast<void*>(avg_src), master, m, v, weights,
+                            const_cast<void*>(ws), s, avg_stride);
+    }));
+    return ok();
+}
+
+DPZ_API int dp_zero1_update(const void* grads, float* master, float* m, float* v, void* weights,
+                            int64_t P, int N, int gdtype, int wdtype, const dpz_adamw_cfg* cfg,
+                            const void* ws, void* stream)
+{
+    return update_common(grads, P, int64_t(N) * P, master, m, v, weights, P, N, gdtype, wdtype,
+                         cfg, ws, stream, "grads");
+}
+
+DPZ_API int dp_zero2_update(const void* shards, float* master, float* m, float* v, void* weights,
+                            int64_t P, int N, int gdtype, int wdtype, const dpz_adamw_cfg* cfg,
+                            const void* ws, void* stream)
+{
+    return update_common(shards, 0, P, master, m, v, weights, P, N, gdtype, wdtype, cfg, ws,
+                         stream, "shards");
 }
 
 DPZ_API int dp_grad_global_norm_static(const void* grads, int64_t P, int N, int gdtype,

@@ -79,10 +79,24 @@ enum class AdamSrc { kLoadOwner, kFold };
 cudaError_t launch_reduce(const Arena& a, const Avg& avg, void* grads, bool all_slabs,
                           void* ws, cudaStream_t s);
 cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaStream_t s);
+
+// A range [lo, hi) of arena elements to reduce: rank r's value of element e
+// at src + r*src_stride + (e - lo), the average of element e (chunk c) stored
+// at dst + c*dst_stride + e (strides and offsets in elements).
+struct RangeArgs {
+    const void* src;
+    int64_t src_stride;
+    void* dst;
+    int64_t dst_stride;
+    int64_t lo, hi;
+};
+cudaError_t launch_reduce_range(const Arena& a, const Avg& avg, const RangeArgs& g, void* ws,
+                                cudaStream_t s);
 cudaError_t launch_norm_finalize(const Arena& a, void* ws, float* norm_out, cudaStream_t s);
 cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                          bool bcast, bool store_avg, void* grads, float* master, float* m,
-                         float* v, void* weights, void* ws, cudaStream_t s);
+                         float* v, void* weights, void* ws, cudaStream_t s,
+                         int64_t avg_stride);
 cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 
 // The fixed device scratch of dp_grad_global_norm_static (norm_static.cu):

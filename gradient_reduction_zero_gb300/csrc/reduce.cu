@@ -173,6 +173,68 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
     }
 }
 
+// Ring-order reduce + average of the arena elements [lo, hi), for a bucket
+// of gradients that is ready before the rest.  Rank r's value of element e is
+// read at src + r*src_stride + (e - lo) and the average of element e (chunk
+// c = e / C) is written at dst + c*dst_stride + e (elements of the gradient
+// dtype).  In place in the arena: src = arena + lo, src_stride = P, dst =
+// arena, dst_stride = P.  From a staging bucket into compact shards (ZeRO-2):
+// src = staging [N][hi - lo], src_stride = hi - lo, dst = shards [P],
+// dst_stride = 0.  Block row y takes the part of the range inside chunk
+// c_first + y.  With SUMSQ the range must start and end on 256-element
+// segment boundaries of its chunks; the partials of those segments are then
+// the ones the whole-arena kernels write.
+template <int GDT, int NT, bool SUMSQ>
+__global__ void __launch_bounds__(kBlock)
+k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restrict__ dst,
+               int64_t dst_stride, int64_t lo, int64_t hi, int64_t C, int n_rt, int c_first,
+               Avg avg, WsHeader* __restrict__ hdr, double* __restrict__ partials)
+{
+    using G = Group<GDT>;
+    constexpr int ES = G::kBytes;
+    const int N = NT > 0 ? NT : n_rt;
+    const int64_t segs = segments_per_chunk(C);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
+    const int64_t sslab = src_stride * ES;
+    if (SUMSQ && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->arrive = 0u;
+    const int c = c_first + (int)blockIdx.y;
+    const int64_t plo = lo > c * C ? lo : c * C;
+    const int64_t phi = hi < (c + 1) * C ? hi : (c + 1) * C;
+    if (plo >= phi) return;
+    const int64_t groups = (phi - plo) / kGroup;
+    const int64_t seg0 = (plo - c * C) / kSegment;          // first segment of the piece
+    for (int64_t wb = first; wb < groups; wb += stride) {
+        const int64_t gi = wb + lane;
+        float ss = 0.0f;
+        if (gi < groups) {
+            const int64_t e = plo + gi * kGroup;
+            const int64_t soff = (e - lo) * ES;
+            float acc[8];
+            if constexpr (NT > 0) {
+                typename G::Raw raw[NT];
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    int r = c + 1 + j;
+                    if (r >= NT) r -= NT;
+                    raw[j] = G::load_raw(src + r * sslab + soff);
+                }
+                fold_loaded<GDT, NT>(raw, acc);
+            } else {
+                ring_fold<GDT>(src, sslab, soff, c, N, acc);
+            }
+            average8<GDT>(acc, avg);
+            if (SUMSQ) ss = sumsq8(acc);
+            G::store_raw(dst + (c * dst_stride + e) * ES, G::pack(acc));
+        }
+        if (SUMSQ) {
+            const float t = warp_sum_f32(ss);
+            if (lane == 0) partials[c * segs + seg0 + wb / 32] = (double)t;
+        }
+    }
+}
+
 // Sums of squares of the owner chunks (chunk c of slab c), per segment.
 template <int GDT>
 __global__ void __launch_bounds__(kBlock)
@@ -304,6 +366,50 @@ cudaError_t launch_reduce(const Arena& a, const Avg& avg, void* grads, bool all_
     if (all_slabs) return reduce_n<0, true, false>(a, avg, grads, ws, s);
     return sumsq ? reduce_n<0, false, true>(a, avg, grads, ws, s)
                  : reduce_n<0, false, false>(a, avg, grads, ws, s);
+}
+
+template <int GDT, int NT, bool SUMSQ>
+static cudaError_t range_t(const Arena& a, const Avg& avg, const RangeArgs& g, void* ws,
+                           cudaStream_t s)
+{
+    auto fn = k_reduce_range<GDT, NT, SUMSQ>;
+    const int c_first = (int)(g.lo / a.C);
+    const int c_last = (int)((g.hi - 1) / a.C);
+    const int pieces = c_last - c_first + 1;
+    int64_t longest = a.C < g.hi - g.lo ? a.C : g.hi - g.lo;
+    dim3 grid = grid_chunks((const void*)fn, longest / kGroup, pieces, 2);
+    grid.y = (unsigned)pieces;
+    set_last_kernel_name(SUMSQ ? "dpz_rs_range_sumsq" : "dpz_rs_range");
+    fn<<<grid, kBlock, 0, s>>>(static_cast<const char*>(g.src), g.src_stride,
+                               static_cast<char*>(g.dst), g.dst_stride, g.lo, g.hi, a.C, a.N,
+                               c_first, avg, static_cast<WsHeader*>(ws),
+                               SUMSQ ? ws_partials(ws) : nullptr);
+    return cudaGetLastError();
+}
+
+template <int GDT, bool SUMSQ>
+static cudaError_t range_n(const Arena& a, const Avg& avg, const RangeArgs& g, void* ws,
+                           cudaStream_t s)
+{
+    switch (a.N) {
+    case 1: return range_t<GDT, 1, SUMSQ>(a, avg, g, ws, s);
+    case 2: return range_t<GDT, 2, SUMSQ>(a, avg, g, ws, s);
+    case 4: return range_t<GDT, 4, SUMSQ>(a, avg, g, ws, s);
+    case 8: return range_t<GDT, 8, SUMSQ>(a, avg, g, ws, s);
+    default: return range_t<GDT, 0, SUMSQ>(a, avg, g, ws, s);
+    }
+}
+
+cudaError_t launch_reduce_range(const Arena& a, const Avg& avg, const RangeArgs& g, void* ws,
+                                cudaStream_t s)
+{
+    const bool sumsq = ws != nullptr;
+    switch (a.gdt) {
+    case 0: return sumsq ? range_n<0, true>(a, avg, g, ws, s) : range_n<0, false>(a, avg, g, ws, s);
+    case 1: return sumsq ? range_n<1, true>(a, avg, g, ws, s) : range_n<1, false>(a, avg, g, ws, s);
+    default:
+        return sumsq ? range_n<2, true>(a, avg, g, ws, s) : range_n<2, false>(a, avg, g, ws, s);
+    }
 }
 
 cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaStream_t s)

@@ -54,6 +54,15 @@ _SIGS = {
                        ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _FP, _VP], ctypes.c_int),
     "dp_grad_global_norm_static": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _FP, _VP],
                                    ctypes.c_int),
+    "dp_reduce_scatter_avg_range": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int64, ctypes.c_int64, _VP, _VP], ctypes.c_int),
+    "dp_reduce_scatter_avg_bucket": ([_VP, ctypes.c_int64, ctypes.c_int64, _VP, ctypes.c_int64,
+                                      ctypes.c_int, ctypes.c_int, _VP, _VP], ctypes.c_int),
+    "dp_grad_norm_finalize": ([_VP, ctypes.c_int64, ctypes.c_int, _FP, _VP], ctypes.c_int),
+    "dp_zero1_update": ([_VP, _FP, _FP, _FP, _VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                         ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _VP], ctypes.c_int),
+    "dp_zero2_update": ([_VP, _FP, _FP, _FP, _VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                         ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _VP], ctypes.c_int),
     "dpz_last_error": ([], ctypes.c_char_p),
     "dpz_version": ([], ctypes.c_char_p),
     "dpz_launch_count": ([], ctypes.c_int64),
@@ -181,6 +190,40 @@ def dp_zero1_step(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None, 
                              _np(grads, N), N, dtype_code(grads, acc32), dtype_code(weights),
                              ctypes.byref(cfg), _ptr(ws), _ptr(norm_out),
                              _stream_handle(stream)))
+
+
+def dp_reduce_scatter_avg_range(grads, N: int, lo: int, n: int, ws=None, stream=None,
+                                acc32: bool = False) -> None:
+    _check(lib.dp_reduce_scatter_avg_range(_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32),
+                                           lo, n, _ptr(ws), _stream_handle(stream)))
+
+
+def dp_reduce_scatter_avg_bucket(staging, lo: int, shards, N: int, ws=None, stream=None,
+                                 acc32: bool = False) -> None:
+    """staging: [N*n] (rank r's values of arena elements [lo, lo+n) at r*n);
+    shards: [P]."""
+    n = _np(staging, N)
+    _check(lib.dp_reduce_scatter_avg_bucket(_ptr(staging), lo, n, _ptr(shards), shards.numel(),
+                                            N, dtype_code(staging, acc32), _ptr(ws),
+                                            _stream_handle(stream)))
+
+
+def dp_grad_norm_finalize(ws, P: int, N: int, norm_out=None, stream=None) -> None:
+    _check(lib.dp_grad_norm_finalize(_ptr(ws), P, N, _ptr(norm_out), _stream_handle(stream)))
+
+
+def dp_zero1_update(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None,
+                    stream=None) -> None:
+    _check(lib.dp_zero1_update(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
+                               _np(grads, N), N, dtype_code(grads), dtype_code(weights),
+                               ctypes.byref(cfg), _ptr(ws), _stream_handle(stream)))
+
+
+def dp_zero2_update(shards, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None,
+                    stream=None) -> None:
+    _check(lib.dp_zero2_update(_ptr(shards), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
+                               shards.numel(), N, dtype_code(shards), dtype_code(weights),
+                               ctypes.byref(cfg), _ptr(ws), _stream_handle(stream)))
 
 
 def launch_count() -> int:

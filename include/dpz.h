@@ -186,6 +186,63 @@ DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v,
                           int wdtype, const dpz_adamw_cfg* cfg, void* ws,
                           float* norm_out, void* stream);
 
+/* ---------------------------------------------------------------------
+ * Buckets (overlap with the backward pass) and ZeRO-2 (sharded gradients)
+ *
+ * A backward pass produces the gradients layer by layer, from the last layer
+ * to the first, so a bucket of the arena can be reduced while the rest is
+ * still being computed ("A4 — Multi-GPU with NCCL and ZeRO-1", Part 3: each
+ * layer's reduction runs on a separate stream after an event recorded on the
+ * compute stream; "Lab 09 — Parallelism, simulated", §2: DDP all-reduces 25
+ * MB buckets as backward produces them; "Distributed training", "Overlap and
+ * graphs").  Record an event on the producing stream after each bucket is
+ * written and make the stream of these calls wait on it.
+ *
+ * Buckets reduce element ranges [lo, lo+n) of the arena (lo and n multiples
+ * of 8; any ranges, in any order, each element once per step).  With ws,
+ * each range must start and end on 256-element segment boundaries of its
+ * chunks ((lo mod C) and ((lo+n) mod C) multiples of 256) and its norm
+ * partials are written; once every bucket is reduced, dp_grad_norm_finalize
+ * gives the same norm, bit for bit, as the whole-arena calls.
+ * ------------------------------------------------------------------- */
+
+/* ZeRO-1 with buckets: reduce + average elements [lo, lo+n) of the arena in
+ * place (the average of element e of chunk c goes to slab c), as
+ * dp_reduce_scatter_avg does for the whole arena.  ws may be NULL (no norm
+ * partials). */
+DPZ_API int dp_reduce_scatter_avg_range(void* grads, int64_t P, int N, int gdtype,
+                                        int64_t lo, int64_t n, void* ws, void* stream);
+
+/* ZeRO-2: gradients are sharded too ("Lab 09", §4: stage 2 shards the
+ * gradients, 2Ψ + 14Ψ/N bytes per rank; "Distributed training":
+ * ZeroSharded[M, N, 2]).  Reduce + average a bucket of N ranks' gradients for
+ * arena elements [lo, lo+n), held in a staging buffer [N][n] (rank r's
+ * values at staging + r*n), into `shards` [P]: the average of element e is
+ * written at shards[e], which belongs to rank e / C's shard.  The staging
+ * buffer can be reused for the next bucket once this call has run, so no
+ * rank keeps a full gradient replica. */
+DPZ_API int dp_reduce_scatter_avg_bucket(const void* staging, int64_t lo, int64_t n,
+                                         void* shards, int64_t P, int N, int gdtype,
+                                         void* ws, void* stream);
+
+/* The global norm from the partials that the range or bucket calls left in
+ * ws (all of [0, P) reduced, with ws); writes it into ws and, if not NULL,
+ * *norm_out. */
+DPZ_API int dp_grad_norm_finalize(void* ws, int64_t P, int N, float* norm_out,
+                                  void* stream);
+
+/* The second half of dp_zero1_step: AdamW on every rank's shard reading the
+ * averaged chunk c of slab c, cast, and the all-gather into all N weight
+ * slabs (one kernel).  Clip scale from the norm in ws when clip_norm > 0. */
+DPZ_API int dp_zero1_update(const void* grads, float* master, float* m, float* v,
+                            void* weights, int64_t P, int N, int gdtype, int wdtype,
+                            const dpz_adamw_cfg* cfg, const void* ws, void* stream);
+
+/* The same for ZeRO-2: the averages are read from shards [P]. */
+DPZ_API int dp_zero2_update(const void* shards, float* master, float* m, float* v,
+                            void* weights, int64_t P, int N, int gdtype, int wdtype,
+                            const dpz_adamw_cfg* cfg, const void* ws, void* stream);
+
 /* The global norm of dp_grad_global_norm for callers that cannot allocate
  * device memory.  The pages have no counterpart to this call.  It serves code
  * that must not call cudaMalloc or any allocator of its own: a plug-in running
