@@ -372,7 +372,8 @@ def run_gpu(args) -> None:
     # ---------------------------------------------------------------- e2e
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, G, step, nrm, stream, world)
+        full = None if w.allreduce_only or w.clip <= 0 else (T, M, V, W, ws, cfg)
+        e2e = run_e2e(args, w, G, step, nrm, stream, world, full)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -518,33 +519,70 @@ def run_graph(args, step, stream, world, nbytes):
             "value": round(nbytes * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT}
 
 
-def run_e2e(args, w, G, step, nrm, stream, world):
-    """Same step through the public API with the gradients coming from pinned
-    host memory and the norm read back, every step."""
+def run_e2e(args, w, G, step, nrm, stream, world, full=None):
+    """The step through the public API with the gradients coming from pinned
+    host memory and the norm read back, every step.  Pipelined: the host-to-
+    device copy of bucket b (a copy engine, one stream) overlaps the reduce-
+    scatter of bucket b-1 (dp_reduce_scatter_avg_range on a second stream,
+    ordered by an event per bucket); then the norm and the update.  The plain
+    form (copy everything, then dp_zero1_step) is timed too."""
     import torch
+    import gradient_reduction_zero_gb300.dpz as dpz
     host = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
     host.copy_(G)
     torch.cuda.synchronize()
+    Gv, Hv = G.view(w.N, w.P), host.view(w.N, w.P)
 
-    def one():
+    def plain():
         G.copy_(host, non_blocking=True)
         step()
         return nrm.item() if not w.allreduce_only else G[:1].item()
 
-    for _ in range(1):
-        one()
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        one()
-    torch.cuda.synchronize()
-    dt = (time.perf_counter() - t0) / args.e2e_steps
-    dt = max_over_ranks(dt, world)
+    copy_s = torch.cuda.Stream()
+    comm = torch.cuda.Stream(priority=-1)
+    buckets = segment_bounds(w.P, w.N, args.e2e_buckets)[::-1]
+
+    def pipelined():
+        T, M, V, W, ws, cfg = full
+        copy_s.wait_stream(stream)
+        comm.wait_stream(stream)
+        for lo, n in buckets:
+            with torch.cuda.stream(copy_s):
+                for r in range(w.N):          # one contiguous DMA copy per rank row
+                    Gv[r, lo:lo + n].copy_(Hv[r, lo:lo + n], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(copy_s)
+            comm.wait_event(ev)
+            dpz.dp_reduce_scatter_avg_range(G, w.N, lo, n, ws=ws, stream=comm)
+        dpz.dp_grad_norm_finalize(ws, w.P, w.N, nrm, stream=comm)
+        dpz.dp_zero1_update(G, T, M, V, W, w.N, cfg, ws=ws, stream=comm)
+        stream.wait_stream(comm)
+        stream.wait_stream(copy_s)
+        return nrm.item()
+
+    def timed(fn):
+        fn()
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            fn()
+        torch.cuda.synchronize()
+        return max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, world)
+
+    dt_plain = timed(plain)
+    use_pipe = full is not None and args.e2e_buckets > 1
+    dt = timed(pipelined) if use_pipe else dt_plain
     d2h = 4 if not w.allreduce_only else G.element_size()
-    return {"value": round(step_bytes(w) * world / dt / 1e9, 2), "unit": UNIT,
-            "ms_per_step": round(dt * 1e3, 3),
-            "h2d_bytes_per_step": G.numel() * G.element_size(), "d2h_bytes_per_step": d2h}
+    out = {"value": round(step_bytes(w) * world / dt / 1e9, 2), "unit": UNIT,
+           "ms_per_step": round(dt * 1e3, 3),
+           "h2d_bytes_per_step": G.numel() * G.element_size(), "d2h_bytes_per_step": d2h,
+           "how": (f"pinned host gradients, {len(buckets)} buckets copied on one stream and "
+                   "reduced on another (dp_reduce_scatter_avg_range, events), then "
+                   "dp_grad_norm_finalize + dp_zero1_update; norm read back")
+           if use_pipe else "pinned host gradients copied, dp_zero1_step, norm read back",
+           "plain_ms_per_step": round(dt_plain * 1e3, 3)}
+    return out
 
 
 def main(argv=None):
@@ -555,6 +593,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["dpz", "reference"], default="dpz")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-buckets", type=int, default=0,
+                    help="> 1: pipeline the e2e host copies with bucketed reduce-scatters")
     ap.add_argument("--buckets", type=int, default=0,
                     help="also measure a bucketed step overlapped with a simulated backward")
     ap.add_argument("--graph", action="store_true",
