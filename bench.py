@@ -301,6 +301,8 @@ def run_gpu(args) -> None:
     import gradient_reduction_zero_gb300.dpz as dpz
 
     w = I.WORKLOADS[args.workload]
+    if args.clip is not None:
+        w = w.with_(clip=args.clip)
     G, T, M, V, W = allocate(w, dev)
     ws = dpz.workspace(w.P, w.N, dev)
     nrm = torch.zeros(1, dtype=torch.float32, device=dev)
@@ -595,6 +597,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-buckets", type=int, default=0,
                     help="> 1: pipeline the e2e host copies with bucketed reduce-scatters")
+    ap.add_argument("--clip", type=float, default=None,
+                    help="override the workload's clip norm (0: no clipping, one fused kernel)")
     ap.add_argument("--buckets", type=int, default=0,
                     help="also measure a bucketed step overlapped with a simulated backward")
     ap.add_argument("--graph", action="store_true",

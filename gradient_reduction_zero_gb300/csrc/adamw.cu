@@ -13,11 +13,12 @@ namespace dpz {
 // Without FOLD the average of element e (chunk c) is read at
 // grads + (c*avg_stride + e) elements: avg_stride = P for the owner slabs of
 // the arena, 0 for a compact [P] buffer of gradient shards.
-// The load-owner variants (no fold) fit 64 registers: four resident blocks
-// per SM keep more loads in flight (measured 94.7 % of the copy peak against
-// 90.5 % with the compiler's 73 registers and three blocks).
+// Register caps that keep more blocks, hence more loads, in flight: the
+// load-owner variants fit 64 registers (four blocks per SM: 94.7 % of the
+// copy peak against 90.5 % with the compiler's 73 registers), the fold
+// variants 80 (three blocks: 95.9 % against 85.5 % with 105 registers).
 template <int GDT, int WDT, int NT, bool FOLD, bool BCAST, bool SUMSQ>
-__global__ void __launch_bounds__(kBlock, FOLD ? 1 : 4)
+__global__ void __launch_bounds__(kBlock, FOLD ? 3 : 4)
 k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
         float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int n_rt,
         Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
@@ -112,10 +113,9 @@ static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bo
                            void* ws, cudaStream_t s, int64_t avg_stride)
 {
     auto fn = k_adamw<GDT, WDT, NT, FOLD, BCAST, SUMSQ>;
-    // the load-owner kernel balances better with many blocks that replace
-    // early finishers (8 waves measured best); the fold kernel is
-    // register-heavier and keeps two waves
-    const dim3 grid = grid_chunks((const void*)fn, a.C / kGroup, a.N, FOLD ? 2 : 8);
+    // blocks that replace early finishers balance the load: 8 waves
+    // measured best for the load-owner kernel, 4 for the fold kernel
+    const dim3 grid = grid_chunks((const void*)fn, a.C / kGroup, a.N, FOLD ? 4 : 8);
     set_last_kernel_name(FOLD ? (SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused")
                               : (BCAST ? "dpz_adamw_bcast" : "dpz_adamw_owner"));
     fn<<<grid, kBlock, 0, s>>>(static_cast<char*>(grads), master, m, v,
