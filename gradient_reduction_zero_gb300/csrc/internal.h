@@ -109,13 +109,10 @@ cudaError_t static_scratch_address(void** ptr);
 const char* last_kernel_name();
 void set_last_kernel_name(const char* name);
 
-// Blocks for a grid-stride kernel: `waves` resident waves (SMs x resident
-// blocks per SM; more than one lets blocks that finish early be replaced),
-// fewer when `threads_needed` is smaller, at most `cap` if cap > 0.
-int grid_for(const void* kernel, int64_t threads_needed, int cap, int waves);
-
 // Grid of a chunk-major streaming kernel: (blocks per chunk, N) when the N
-// chunks fit side by side in `waves` resident waves, else (wave, 1).
+// chunks fit side by side in `waves` resident waves (SMs x resident blocks
+// per SM; more than one wave lets blocks that finish early be replaced),
+// else (waves x that, 1).
 dim3 grid_chunks(const void* kernel, int64_t threads_per_chunk, int N, int waves);
 
 }  // namespace dpz

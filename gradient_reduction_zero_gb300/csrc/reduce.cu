@@ -5,7 +5,9 @@
 // All streaming kernels use the same mapping: chunk-major, and inside chunk c
 // a grid-stride loop over 8-element groups, so every thread of a warp works on
 // the same chunk (uniform ring order) and consecutive threads touch
-// consecutive 16-byte words of every slab (coalesced).
+// consecutive 16- or 32-byte words of every slab (coalesced).  Block row y
+// takes chunks y, y + gridDim.y, ... (one row for large arenas, N rows when
+// the chunks are small enough to run side by side).
 #include <mutex>
 #include <unordered_map>
 
@@ -57,17 +59,6 @@ int blocks_per_sm(const void* fn)
 
 }  // namespace
 
-// `waves` resident waves (SMs x blocks per SM), fewer if the chunk is short.
-int grid_for(const void* fn, int64_t threads_needed, int cap, int waves)
-{
-    int64_t g = (int64_t)device_sms() * blocks_per_sm(fn) * (waves < 1 ? 1 : waves);
-    int64_t need = (threads_needed + kBlock - 1) / kBlock;
-    if (need < g) g = need;
-    if (cap > 0 && g > cap) g = cap;
-    if (g < 1) g = 1;
-    return (int)g;
-}
-
 // Grid of a chunk-major streaming kernel.  When the blocks that one chunk
 // needs, times N, fit in `waves` resident waves, every chunk gets its own
 // row of blocks (grid.y = N) and the chunks run side by side; otherwise a
@@ -86,9 +77,10 @@ void set_last_kernel_name(const char* n) { g_last_kernel = n; }
 
 // ------------------------------------------------------------------ kernels
 //
-// Loop shape shared by the streaming kernels: for chunk c = 0..N-1, each warp
-// walks warp-iterations wb = first, first + stride, ... (32 consecutive
-// groups of 8 elements, all lanes together), lane l taking group wb + l.
+// Loop shape shared by the streaming kernels: for each chunk c of the block's
+// row, each warp walks warp-iterations wb = first, first + stride, ... (32
+// consecutive groups of 8 elements, all lanes together), lane l taking group
+// wb + l.
 // Kernels that produce norm partials write, for every warp-iteration, the sum
 // of squares of its 256 averaged elements (fixed shuffle tree) into the slot
 // of that segment, so the partials do not depend on the grid.

@@ -350,3 +350,28 @@ def test_acc32_fused_equals_unfused(clip):
     for x, y in zip(a[:5], b[:5]):
         assert same_bits(x, y)
     assert a[5] == b[5]
+
+
+def test_resume_from_saved_state():
+    """The library keeps no state: saving master/m/v/weights and the step
+    counter, then continuing from fresh buffers, equals running on."""
+    N, C = 4, 2056
+    w, g, th, m, v, wts = make_problem(N, C, "bf16", "bf16", 1e-3, seed=21, step=1)
+    m[:] = 0
+    v[:] = 0
+    grads = [I.arena_host(w.with_(grad_seed=100 * t)) for t in (1, 2, 3)]
+
+    def run(state, steps):
+        T, M, V, W = (up(x) for x in state)
+        ws = dpz.workspace(w.P, N, DEV)
+        for t in steps:
+            cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, t, w.clip)
+            dpz.dp_zero1_step(up(grads[t - 1]), T, M, V, W, N, cfg, ws=ws)
+        torch.cuda.synchronize()
+        return [down(x) for x in (T, M, V, W)]
+
+    straight = run((th, m, v, wts), (1, 2, 3))
+    saved = run((th, m, v, wts), (1, 2))            # a checkpoint after step 2
+    resumed = run(saved, (3,))
+    for a, b in zip(straight, resumed):
+        assert same_bits(a, b)
