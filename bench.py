@@ -292,6 +292,59 @@ def allocate(w: I.Workload, dev):
     return G, T, M, V, W
 
 
+ENTRIES = ("step", "reduce_scatter", "allreduce", "norm", "adamw_owner", "allgather", "update",
+           "range", "bucket_zero2", "norm_static")
+
+
+def entry_bytes(entry: str, w: I.Workload) -> int:
+    """Algorithmic bytes of one call of a single entry point."""
+    N, P, eg, ew = w.N, w.P, w.grad_bytes(), w.weight_bytes()
+    return {"reduce_scatter": N * P * eg + P * eg,
+            "range": N * P * eg + P * eg,
+            "bucket_zero2": N * P * eg + P * eg,
+            "allreduce": 2 * N * P * eg,
+            "norm": P * eg, "norm_static": P * eg,
+            "adamw_owner": P * eg + 24 * P + P * ew,
+            "update": P * eg + 24 * P + N * P * ew,
+            "allgather": N * P * ew}[entry]
+
+
+def entry_op(args, w, dpz, G, T, M, V, W, ws, nrm, cfg, stream):
+    """One entry point alone, on the workload's buffers (for per-kernel timing
+    and profiling).  Every call computes real results from the previous one's
+    buffers; the bytes are the same each time."""
+    import torch
+    N, P = w.N, w.P
+    if args.entry == "bucket_zero2":
+        shards = torch.empty(P, dtype=G.dtype, device=G.device)
+    if args.entry == "allreduce":
+        return lambda on=None: dpz.dp_allreduce_avg(G, N, on or stream, acc32=args.acc32)
+    if args.entry == "reduce_scatter":
+        return lambda on=None: dpz.dp_reduce_scatter_avg(G, N, on or stream, acc32=args.acc32)
+    if args.entry == "range":
+        return lambda on=None: dpz.dp_reduce_scatter_avg_range(G, N, 0, P, ws=ws,
+                                                               stream=on or stream,
+                                                               acc32=args.acc32)
+    if args.entry == "bucket_zero2":
+        # the whole arena as one bucket: staging = the arena, shards = [P]
+        return lambda on=None: dpz.dp_reduce_scatter_avg_bucket(G, 0, shards, N, ws=ws,
+                                                                stream=on or stream,
+                                                                acc32=args.acc32)
+    if args.entry == "norm":
+        return lambda on=None: dpz.dp_grad_global_norm(G, N, ws, nrm, stream=on or stream)
+    if args.entry == "norm_static":
+        return lambda on=None: dpz.dp_grad_global_norm_static(G, N, nrm, stream=on or stream)
+    if args.entry == "adamw_owner":
+        return lambda on=None: dpz.zero1_adamw_step(G, T, M, V, W, N, cfg, ws=ws,
+                                                    stream=on or stream)
+    if args.entry == "update":
+        return lambda on=None: dpz.dp_zero1_update(G, T, M, V, W, N, cfg, ws=ws,
+                                                   stream=on or stream)
+    if args.entry == "allgather":
+        return lambda on=None: dpz.dp_allgather(W, N, on or stream)
+    raise ValueError(args.entry)
+
+
 def run_gpu(args) -> None:
     import torch
 
@@ -309,13 +362,22 @@ def run_gpu(args) -> None:
     cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)
     stream = torch.cuda.current_stream()
 
-    def step(on=None):
+    def full_step(on=None):
         on = stream if on is None else on
         if w.allreduce_only:
             dpz.dp_allreduce_avg(G, w.N, on, acc32=args.acc32)
         else:
             dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=on,
                               acc32=args.acc32)
+
+    step = full_step
+    if args.entry != "step":
+        # one full step first leaves a valid norm in the workspace
+        if not w.allreduce_only:
+            full_step()
+        step = entry_op(args, w, dpz, G, T, M, V, W, ws, nrm, cfg, stream)
+        args.no_e2e = args.no_cpu_baseline = True
+        args.buckets = 0
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -346,7 +408,7 @@ def run_gpu(args) -> None:
     ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(ms, world)
 
-    nbytes = step_bytes(w)
+    nbytes = step_bytes(w) if args.entry == "step" else entry_bytes(args.entry, w)
     value = nbytes * world / (ms_max * 1e-3) / 1e9
     pk = peaks()
 
@@ -354,7 +416,7 @@ def run_gpu(args) -> None:
     dom = max(kstats.items(), key=lambda kv: kv[1][1])
     dname, (dn, dms) = dom
     per_launch_ms = dms / dn
-    kb = kernel_bytes(dname, w)
+    kb = kernel_bytes(dname, w) if args.entry == "step" else entry_bytes(args.entry, w)
     achieved = kb / (per_launch_ms * 1e-3) / 1e9
     shares = {k: {"launches": n, "ms_total": round(t, 4),
                   "share": round(t / sum(x[1] for x in kstats.values()), 4)}
@@ -386,7 +448,7 @@ def run_gpu(args) -> None:
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_max, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": config_of(w, args.acc32),
+            "data": "synthetic", "config": dict(config_of(w, args.acc32), entry=args.entry),
             "steps_per_s": round(1e3 / ms_max, 3),
             "pct_of_hbm_roofline": {
                 "measured_copy_peak": round(100 * value / world / pk["hbm_gbs"], 2),
@@ -597,6 +659,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-buckets", type=int, default=0,
                     help="> 1: pipeline the e2e host copies with bucketed reduce-scatters")
+    ap.add_argument("--entry", choices=ENTRIES, default="step",
+                    help="time one entry point alone instead of the whole step")
     ap.add_argument("--clip", type=float, default=None,
                     help="override the workload's clip norm (0: no clipping, one fused kernel)")
     ap.add_argument("--buckets", type=int, default=0,
