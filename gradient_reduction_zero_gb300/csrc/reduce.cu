@@ -227,6 +227,14 @@ k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restric
     }
 }
 
+// Segments per warp-iteration for the single-stream kernels (norm of the
+// owner chunks, all-gather): one 16- or 32-byte load per lane and segment, so
+// several segments keep enough bytes in flight.
+template <int DT>
+struct StreamSegs {
+    static constexpr int value = DT == 0 ? 2 : 4;
+};
+
 // Sums of squares of the owner chunks (chunk c of slab c), per segment.
 template <int GDT>
 __global__ void __launch_bounds__(kBlock)
@@ -234,6 +242,7 @@ k_norm_owned(const char* __restrict__ grads, int64_t P, int64_t C, int N,
              WsHeader* __restrict__ hdr, double* __restrict__ partials)
 {
     constexpr int ES = Group<GDT>::kBytes;
+    constexpr int U = StreamSegs<GDT>::value;
     const int64_t slab = P * ES;
     const int64_t groups = C / kGroup;
     const int64_t segs = segments_per_chunk(C);
@@ -242,16 +251,28 @@ k_norm_owned(const char* __restrict__ grads, int64_t P, int64_t C, int N,
     const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     for (int c = blockIdx.y; c < N; c += gridDim.y) {
-        for (int64_t wb = first; wb < groups; wb += stride) {
-            const int64_t gi = wb + lane;
-            float ss = 0.0f;
-            if (gi < groups) {
-                float x[8];
-                load_group<GDT>(grads + c * slab + (c * C + gi * kGroup) * ES, x);
-                ss = sumsq8(x);
+        const char* base = grads + c * slab + c * C * ES;
+        for (int64_t wb0 = first * U; wb0 < groups; wb0 += stride * U) {
+            typename Group<GDT>::Raw raw[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t gi = wb0 + 32 * u + lane;
+                if (gi < groups) raw[u] = Group<GDT>::load_raw(base + gi * kGroup * ES);
             }
-            const float t = warp_sum_f32(ss);
-            if (lane == 0) partials[c * segs + wb / 32] = (double)t;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t wb = wb0 + 32 * u;
+                float ss = 0.0f;
+                if (wb + lane < groups) {
+                    float x[8];
+                    Group<GDT>::unpack(raw[u], x);
+                    ss = sumsq8(x);
+                }
+                if (wb < groups) {
+                    const float t = warp_sum_f32(ss);
+                    if (lane == 0) partials[c * segs + wb / 32] = (double)t;
+                }
+            }
         }
     }
 }
@@ -301,16 +322,28 @@ __global__ void __launch_bounds__(kBlock)
 k_allgather(char* __restrict__ w, int64_t P, int64_t C, int N)
 {
     constexpr int ES = Group<WDT>::kBytes;
+    constexpr int U = StreamSegs<WDT>::value;
     const int64_t slab = P * ES;
     const int64_t groups = C / kGroup;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
     for (int c = blockIdx.y; c < N; c += gridDim.y) {
-        for (int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; gi < groups;
-             gi += stride) {
-            const int64_t off = (c * C + gi * kGroup) * ES;
-            const typename Group<WDT>::Raw x = Group<WDT>::load_raw(w + c * slab + off);
-            for (int r = 0; r < N; ++r)
-                if (r != c) Group<WDT>::store_raw(w + r * slab + off, x);
+        const int64_t c0 = c * C * ES;
+        for (int64_t wb0 = first * U; wb0 < groups; wb0 += stride * U) {
+            typename Group<WDT>::Raw x[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t gi = wb0 + 32 * u + lane;
+                if (gi < groups) x[u] = Group<WDT>::load_raw(w + c * slab + c0 + gi * kGroup * ES);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t gi = wb0 + 32 * u + lane;
+                if (gi < groups)
+                    for (int r = 0; r < N; ++r)
+                        if (r != c) Group<WDT>::store_raw(w + r * slab + c0 + gi * kGroup * ES, x[u]);
+            }
         }
     }
 }
@@ -410,10 +443,12 @@ cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaS
     const char* g = static_cast<const char*>(grads);
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     if (a.gdt != 0) {      // both bf16 modes store bf16 averages
-        const dim3 grid = grid_chunks((const void*)k_norm_owned<1>, a.C / kGroup, a.N, 2);
+        const dim3 grid = grid_chunks((const void*)k_norm_owned<1>,
+                                      a.C / kGroup / StreamSegs<1>::value, a.N, 2);
         k_norm_owned<1><<<grid, kBlock, 0, s>>>(g, a.P, a.C, a.N, hdr, ws_partials(ws));
     } else {
-        const dim3 grid = grid_chunks((const void*)k_norm_owned<0>, a.C / kGroup, a.N, 2);
+        const dim3 grid = grid_chunks((const void*)k_norm_owned<0>,
+                                      a.C / kGroup / StreamSegs<0>::value, a.N, 2);
         k_norm_owned<0><<<grid, kBlock, 0, s>>>(g, a.P, a.C, a.N, hdr, ws_partials(ws));
     }
     return cudaGetLastError();
@@ -437,10 +472,12 @@ cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s)
     set_last_kernel_name("dpz_allgather");
     char* w = static_cast<char*>(weights);
     if (a.wdt == 1) {
-        const dim3 grid = grid_chunks((const void*)k_allgather<1>, a.C / kGroup, a.N, 2);
+        const dim3 grid = grid_chunks((const void*)k_allgather<1>,
+                                      a.C / kGroup / StreamSegs<1>::value, a.N, 2);
         k_allgather<1><<<grid, kBlock, 0, s>>>(w, a.P, a.C, a.N);
     } else {
-        const dim3 grid = grid_chunks((const void*)k_allgather<0>, a.C / kGroup, a.N, 2);
+        const dim3 grid = grid_chunks((const void*)k_allgather<0>,
+                                      a.C / kGroup / StreamSegs<0>::value, a.N, 2);
         k_allgather<0><<<grid, kBlock, 0, s>>>(w, a.P, a.C, a.N);
     }
     return cudaGetLastError();
