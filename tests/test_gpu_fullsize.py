@@ -1,5 +1,6 @@
-"""GPU parity at the workloads' full sizes, in the launch configuration the
-benchmark times (dp_zero1_step with clip, workspace and norm output;
+"""GPU parity at the workloads' full sizes, in the launch configurations the
+benchmark times (dp_zero1_step with clip, workspace and norm output; also
+without clip, the one-kernel step, and with the fp32-accumulating ring;
 dp_allreduce_avg for the all-reduce workloads).  The oracle computes sampled
 windows of every chunk one by one (the start, the middle and the ragged end)
 and the global norm over the whole arena, window by window on host threads;
@@ -30,7 +31,7 @@ def window_offsets(C):
     return sorted({0, (C // 2) // 8 * 8, C - WIDTH})
 
 
-def oracle_full_sumsq(w, width=1 << 20):
+def oracle_full_sumsq(w, width=1 << 20, acc32=False):
     """Sum of squares of the averaged gradient of the whole arena: the oracle's
     reduce-scatter, average and sum of squares on every window, added with
     math.fsum (the sum of squares is additive over windows)."""
@@ -39,8 +40,7 @@ def oracle_full_sumsq(w, width=1 << 20):
     def part(o):
         wd = min(width, C - o)
         g = I.window_arena_host(w, o, wd)
-        O.ring_reduce_scatter(g)
-        O.average_owned(g)
+        O.reduce_scatter_avg(g, acc32=acc32)
         return O.sumsq_owned(g)
 
     with ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
@@ -58,8 +58,13 @@ def gpu_state_window(t, N, C, o, wd):
     return np.concatenate([down(t[c * C + o:c * C + o + wd]) for c in range(N)])
 
 
-@pytest.mark.parametrize("w", [I.GPT2_124M, I.GPT2_1P5B], ids=lambda w: w.name)
-def test_zero1_step_full_size(w):
+@pytest.mark.parametrize("w,acc32", [(I.GPT2_124M, False), (I.GPT2_1P5B, False),
+                                     (I.GPT2_1P5B.with_(clip=0.0), False),
+                                     (I.GPT2_124M, True)],
+                         ids=["gpt2-124m", "gpt2-1.5b", "gpt2-1.5b-no-clip", "gpt2-124m-acc32"])
+def test_zero1_step_full_size(w, acc32):
+    """The clipped three-kernel step, the one-kernel step without clipping,
+    and the fp32-accumulating ring, at full size."""
     N, P, C = w.N, w.P, w.C
     gd = torch.bfloat16
     G = torch.empty(N * P, dtype=gd, device=DEV)
@@ -71,15 +76,17 @@ def test_zero1_step_full_size(w):
     W = torch.zeros(N * P, dtype=gd, device=DEV)
     ws = dpz.workspace(P, N, DEV)
     nrm = torch.zeros(1, device=DEV)
-    cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)
-    dpz.dp_zero1_step(G, T, M, V, W, N, cfg, ws=ws, norm_out=nrm)
+    cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip,
+                       store_avg=True)
+    dpz.dp_zero1_step(G, T, M, V, W, N, cfg, ws=ws, norm_out=nrm, acc32=acc32)
     torch.cuda.synchronize()
     gnorm = nrm.item()
 
-    ss = oracle_full_sumsq(w)
+    ss = oracle_full_sumsq(w, acc32=acc32)
     onorm, oscale = O.clip_scale(ss, w.clip)
     assert abs(gnorm - onorm) <= 1e-6 * onorm, (gnorm, onorm)
-    assert oscale < 1.0                           # the clip is active
+    if w.clip > 0:
+        assert oscale < 1.0                       # the clip is active
 
     ocfg = O.cfg_from_workload(w)
     for o in window_offsets(C):
@@ -89,7 +96,7 @@ def test_zero1_step_full_size(w):
         v = I.window_state_host(w, "v", o, WIDTH)
         wt = np.zeros((N, N * WIDTH), dtype=np.uint16)
         G1, T1, M1, V1, W1 = g.copy(), th.copy(), m.copy(), v.copy(), wt.copy()
-        n1, s1, _, _ = O.zero1_step(G1, T1, M1, V1, W1, ocfg, ext_sumsq=ss)
+        n1, s1, _, _ = O.zero1_step(G1, T1, M1, V1, W1, ocfg, ext_sumsq=ss, acc32=acc32)
         assert n1 == onorm
         Gg = gpu_window(G, N, P, C, o, WIDTH)
         Wg = gpu_window(W, N, P, C, o, WIDTH)
@@ -103,7 +110,7 @@ def test_zero1_step_full_size(w):
                 assert same_bits(Gg[r, sl], want), (o, r, c)
         for r in range(N):
             assert same_bits(Wg[r], Wg[0])
-        if gnorm == onorm:
+        if gnorm == onorm or w.clip <= 0:
             assert same_bits(Tg, T1) and same_bits(Mg, M1) and same_bits(Vg, V1)
             assert same_bits(Wg, W1)
         else:
