@@ -163,8 +163,7 @@ static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, A
                                         s);
     }
     if (bcast)
-        return adamw_t<GDT, WDT, 0, false, true, false>(a, avg, h, false, grads, master, m, v,
-                                                       weights, ws, s, avg_stride);
+        return launch_adamw_bcast_tma(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     return adamw_t<GDT, WDT, 0, false, false, false>(a, avg, h, false, grads, master, m, v,
                                                     weights, ws, s, avg_stride);
 }

@@ -28,20 +28,6 @@ std::mutex g_mu;
 std::unordered_map<int, DevInfo> g_dev;
 std::unordered_map<const void*, int> g_occ;   // kernel -> resident blocks per SM
 
-int device_sms()
-{
-    int dev = 0;
-    cudaGetDevice(&dev);
-    std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_dev.find(dev);
-    if (it != g_dev.end()) return it->second.sms;
-    DevInfo d;
-    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    if (d.sms <= 0) d.sms = 1;
-    g_dev[dev] = d;
-    return d.sms;
-}
-
 int blocks_per_sm(const void* fn)
 {
     {
@@ -58,6 +44,20 @@ int blocks_per_sm(const void* fn)
 }
 
 }  // namespace
+
+int device_sms()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_dev.find(dev);
+    if (it != g_dev.end()) return it->second.sms;
+    DevInfo d;
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (d.sms <= 0) d.sms = 1;
+    g_dev[dev] = d;
+    return d.sms;
+}
 
 // Grid of a chunk-major streaming kernel.  When the blocks that one chunk
 // needs, times N, fit in `waves` resident waves, every chunk gets its own
