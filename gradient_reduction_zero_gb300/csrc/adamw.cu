@@ -13,12 +13,17 @@ namespace dpz {
 // Without FOLD the average of element e (chunk c) is read at
 // grads + (c*avg_stride + e) elements: avg_stride = P for the owner slabs of
 // the arena, 0 for a compact [P] buffer of gradient shards.
-// Register caps that keep more blocks, hence more loads, in flight: the
-// load-owner variants fit 64 registers (four blocks per SM: 94.7 % of the
-// copy peak against 90.5 % with the compiler's 73 registers), the fold
-// variants 80 (three blocks: 95.9 % against 85.5 % with 105 registers).
+// One-shot grid, one segment per warp (device.cuh).  Register caps that keep
+// more blocks, hence more loads, in flight: 64 registers (four blocks per SM)
+// wherever that does not spill, which is every load-owner variant and the
+// fold over up to four bf16 slabs; 80 (three blocks) for the other folds.
+template <int GDT, int NT, bool FOLD>
+struct AdamwBlocksPerSm {
+    static constexpr int value = !FOLD || (GDT != 0 && NT > 0 && NT <= 4) ? 4 : 3;
+};
+
 template <int GDT, int WDT, int NT, bool FOLD, bool BCAST, bool SUMSQ>
-__global__ void __launch_bounds__(kBlock, FOLD ? 3 : 4)
+__global__ void __launch_bounds__(kBlock, AdamwBlocksPerSm<GDT, NT, FOLD>::value)
 k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
         float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int n_rt,
         Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
@@ -30,7 +35,14 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
     const int64_t gslab = P * GES;
     const int64_t wslab = P * WES;
     const int64_t groups = C / kGroup;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t segs = segments_per_chunk(C);
+    const int lane = threadIdx.x & 31;
+    if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
+    const int64_t sw = global_warp();
+    if (sw >= (int64_t)N * segs) return;                 // whole warps
+    const SegPos p = seg_pos(sw, segs);
+    const int c = p.c;
+    const int64_t gi = p.seg * 32 + lane;
 
     // clip scale from the global norm of the averaged gradient
     float scale = 1.0f;
@@ -43,67 +55,57 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
         }
     }
 
-    const int64_t segs = segments_per_chunk(C);
-    const int lane = threadIdx.x & 31;
-    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x - lane;
-    if (SUMSQ && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->arrive = 0u;
-    for (int c = blockIdx.y; c < N; c += gridDim.y) {
+    float ss = 0.0f;
+    if (gi < groups) {
+        const int64_t e = c * C + gi * kGroup;  // element index (same in every slab)
         constexpr int NS = NT > 0 ? NT : 1;
         const char* src[NS];
         if constexpr (NT > 0) ring_sources<NT>(grads, gslab, c, src);
-        for (int64_t wb = first; wb < groups; wb += stride) {
-            const int64_t gi = wb + lane;
-            float ss = 0.0f;
-            if (gi < groups) {
-                const int64_t e = c * C + gi * kGroup;  // element index (same in every slab)
-                float g[8];
-                if (FOLD) {
-                    if constexpr (NT > 0) {
-                        typename Group<GDT>::Raw raw[NT];
+        float g[8];
+        if (FOLD) {
+            if constexpr (NT > 0) {
+                typename Group<GDT>::Raw raw[NT];
 #pragma unroll
-                        for (int j = 0; j < NT; ++j)
-                            raw[j] = Group<GDT>::load_raw(src[j] + e * GES);
-                        fold_loaded<GDT, NT>(raw, g);
-                    } else {
-                        ring_fold<GDT>(grads, gslab, e * GES, c, N, g);
-                    }
-                    average8<GDT>(g, avg);
-                    if (SUMSQ) ss = sumsq8(g);
-                    if (store_avg) store_group<GDT>(grads + c * gslab + e * GES, g);
-                } else {
-                    load_group<GDT>(grads + (c * avg_stride + e) * GES, g);
-                }
-                float th[8], mm[8], vv[8];
-                load_group<0>(reinterpret_cast<const char*>(master + e), th);
-                load_group<0>(reinterpret_cast<const char*>(mom + e), mm);
-                load_group<0>(reinterpret_cast<const char*>(var + e), vv);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float gq = do_scale ? __fmul_rn(g[q], scale) : g[q];
-                    adamw_elem(th[q], mm[q], vv[q], gq, h);
-                }
-                store_group<0>(reinterpret_cast<char*>(master + e), th);
-                store_group<0>(reinterpret_cast<char*>(mom + e), mm);
-                store_group<0>(reinterpret_cast<char*>(var + e), vv);
-                const typename Group<WDT>::Raw w = Group<WDT>::pack(th);
-                if (BCAST) {
-                    if constexpr (NT > 0) {
-#pragma unroll
-                        for (int r = 0; r < NT; ++r)
-                            Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
-                    } else {
-                        for (int r = 0; r < N; ++r)
-                            Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
-                    }
-                } else {
-                    Group<WDT>::store_raw(weights + c * wslab + e * WES, w);
-                }
+                for (int j = 0; j < NT; ++j) raw[j] = Group<GDT>::load_raw(src[j] + e * GES);
+                fold_loaded<GDT, NT>(raw, g);
+            } else {
+                ring_fold<GDT>(grads, gslab, e * GES, c, N, g);
             }
-            if (SUMSQ) {                      // wb < groups: uniform over the warp
-                const float t = warp_sum_f32(ss);
-                if (lane == 0) partials[c * segs + wb / 32] = (double)t;
-            }
+            average8<GDT>(g, avg);
+            if (SUMSQ) ss = sumsq8(g);
+            if (store_avg) store_group<GDT>(grads + c * gslab + e * GES, g);
+        } else {
+            load_group<GDT>(grads + (c * avg_stride + e) * GES, g);
         }
+        float th[8], mm[8], vv[8];
+        load_group<0>(reinterpret_cast<const char*>(master + e), th);
+        load_group<0>(reinterpret_cast<const char*>(mom + e), mm);
+        load_group<0>(reinterpret_cast<const char*>(var + e), vv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float gq = do_scale ? __fmul_rn(g[q], scale) : g[q];
+            adamw_elem(th[q], mm[q], vv[q], gq, h);
+        }
+        store_group<0>(reinterpret_cast<char*>(master + e), th);
+        store_group<0>(reinterpret_cast<char*>(mom + e), mm);
+        store_group<0>(reinterpret_cast<char*>(var + e), vv);
+        const typename Group<WDT>::Raw w = Group<WDT>::pack(th);
+        if (BCAST) {
+            if constexpr (NT > 0) {
+#pragma unroll
+                for (int r = 0; r < NT; ++r)
+                    Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
+            } else {
+                for (int r = 0; r < N; ++r)
+                    Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
+            }
+        } else {
+            Group<WDT>::store_raw(weights + c * wslab + e * WES, w);
+        }
+    }
+    if (SUMSQ) {
+        const float t = warp_sum_f32(ss);
+        if (lane == 0) partials[c * segs + p.seg] = (double)t;
     }
 }
 
@@ -112,16 +114,13 @@ static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bo
                            void* grads, float* master, float* m, float* v, void* weights,
                            void* ws, cudaStream_t s, int64_t avg_stride)
 {
-    auto fn = k_adamw<GDT, WDT, NT, FOLD, BCAST, SUMSQ>;
-    // blocks that replace early finishers balance the load: 8 waves
-    // measured best for the load-owner kernel, 4 for the fold kernel
-    const dim3 grid = grid_chunks((const void*)fn, a.C / kGroup, a.N, FOLD ? 4 : 8);
+    const unsigned blocks = blocks_for_segments(int64_t(a.N) * segments_per_chunk(a.C), 1);
     set_last_kernel_name(FOLD ? (SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused")
                               : (BCAST ? "dpz_adamw_bcast" : "dpz_adamw_owner"));
-    fn<<<grid, kBlock, 0, s>>>(static_cast<char*>(grads), master, m, v,
-                               static_cast<char*>(weights), a.P, a.C, a.N, avg, h,
-                               store_avg ? 1 : 0, static_cast<WsHeader*>(ws),
-                               SUMSQ ? ws_partials(ws) : nullptr, avg_stride);
+    k_adamw<GDT, WDT, NT, FOLD, BCAST, SUMSQ><<<blocks, kBlock, 0, s>>>(
+        static_cast<char*>(grads), master, m, v, static_cast<char*>(weights), a.P, a.C, a.N, avg,
+        h, store_avg ? 1 : 0, static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr,
+        avg_stride);
     return cudaGetLastError();
 }
 
@@ -150,6 +149,30 @@ static cudaError_t fused_n(const Arena& a, const Avg& avg, const AdamArgs& h, bo
 }
 
 template <int GDT, int WDT>
+static cudaError_t bcast_n(const Arena& a, const Avg& avg, const AdamArgs& h, void* grads,
+                           float* master, float* m, float* v, void* weights, void* ws,
+                           cudaStream_t s, int64_t avg_stride)
+{
+    switch (a.N) {
+    case 1:
+        return adamw_t<GDT, WDT, 1, false, true, false>(a, avg, h, false, grads, master, m, v,
+                                                        weights, ws, s, avg_stride);
+    case 2:
+        return adamw_t<GDT, WDT, 2, false, true, false>(a, avg, h, false, grads, master, m, v,
+                                                        weights, ws, s, avg_stride);
+    case 4:
+        return adamw_t<GDT, WDT, 4, false, true, false>(a, avg, h, false, grads, master, m, v,
+                                                        weights, ws, s, avg_stride);
+    case 8:
+        return adamw_t<GDT, WDT, 8, false, true, false>(a, avg, h, false, grads, master, m, v,
+                                                        weights, ws, s, avg_stride);
+    default:
+        return adamw_t<GDT, WDT, 0, false, true, false>(a, avg, h, false, grads, master, m, v,
+                                                        weights, ws, s, avg_stride);
+    }
+}
+
+template <int GDT, int WDT>
 static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                             bool bcast, bool store_avg, void* grads, float* master, float* m,
                             float* v, void* weights, void* ws, cudaStream_t s,
@@ -163,7 +186,7 @@ static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, A
                                         s);
     }
     if (bcast)
-        return launch_adamw_bcast_tma(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+        return bcast_n<GDT, WDT>(a, avg, h, grads, master, m, v, weights, ws, s, avg_stride);
     return adamw_t<GDT, WDT, 0, false, false, false>(a, avg, h, false, grads, master, m, v,
                                                     weights, ws, s, avg_stride);
 }

@@ -99,14 +99,6 @@ cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, Adam
                          int64_t avg_stride);
 cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 
-// AdamW + cast + all-gather from the stored averages (element e of chunk c
-// at grads + c*avg_stride + e), staged through shared memory by bulk copies
-// (adamw_tma.cu).  A tile that does not arrive within the wait limit sets the
-// device error flag that read_and_clear_pipeline_error returns.
-cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
-                                   int64_t avg_stride, float* master, float* m, float* v,
-                                   void* weights, const void* ws, cudaStream_t s);
-cudaError_t read_and_clear_pipeline_error(unsigned* flag);
 
 // The fixed device scratch of dp_grad_global_norm_static (norm_static.cu):
 // its size in bytes, and its device address on the current device (looked
@@ -118,13 +110,13 @@ cudaError_t static_scratch_address(void** ptr);
 const char* last_kernel_name();
 void set_last_kernel_name(const char* name);
 
-// Streaming multiprocessors of the current device (cached per device).
-int device_sms();
-
-// Grid of a chunk-major streaming kernel: (blocks per chunk, N) when the N
-// chunks fit side by side in `waves` resident waves (SMs x resident blocks
-// per SM; more than one wave lets blocks that finish early be replaced),
-// else (waves x that, 1).
-dim3 grid_chunks(const void* kernel, int64_t threads_per_chunk, int N, int waves);
+// Blocks of kBlock threads for a one-shot grid over `segments` 256-element
+// segments, U per warp.
+inline unsigned blocks_for_segments(int64_t segments, int U)
+{
+    const int64_t per_block = int64_t(U) * (kBlock / 32);
+    const int64_t b = (segments + per_block - 1) / per_block;
+    return (unsigned)(b < 1 ? 1 : b);
+}
 
 }  // namespace dpz

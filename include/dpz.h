@@ -271,17 +271,6 @@ DPZ_API const char* dpz_last_error(void);
 /* Library version string. */
 DPZ_API const char* dpz_version(void);
 
-/* Device-side error flag of the current device, read and cleared.  Kernels
- * that wait on their own asynchronous copies (the AdamW + all-gather kernel of
- * dp_zero1_step with clipping, dp_zero1_update and dp_zero2_update) bound
- * every wait by the SM clock (about two seconds); a wait that runs out stops
- * the kernel early, leaves its outputs incomplete, and sets this flag instead
- * of hanging.  *flag_out = 1 if that happened since the last call, else 0.
- * Synchronous: call it after the work in question has finished (for example
- * after cudaStreamSynchronize), not inside a stream capture.  Returns
- * DPZ_ERR_INVALID_ARG for a NULL flag_out, DPZ_ERR_CUDA if the read fails. */
-DPZ_API int dpz_device_status(int* flag_out);
-
 /* Number of kernels this library has launched since it was loaded. */
 DPZ_API int64_t dpz_launch_count(void);
 
