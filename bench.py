@@ -497,7 +497,8 @@ def run_buckets(args, w, G, T, M, V, W, ws, nrm, cfg, stream, rs_ms):
     generator, last bucket first) on the main stream.  Serial: the whole
     backward, then dp_zero1_step.  Overlapped: after each bucket an event;
     a second stream waits on it and reduces that bucket
-    (dp_reduce_scatter_avg_range), then finalises the norm and runs
+    (dp_reduce_scatter_avg_range, capped at one block per SM so that the
+    backward keeps most of the GPU), then finalises the norm and runs
     dp_zero1_update once the last bucket is in.  Both compute the same step."""
     import torch
     import gradient_reduction_zero_gb300.dpz as dpz
@@ -508,6 +509,7 @@ def run_buckets(args, w, G, T, M, V, W, ws, nrm, cfg, stream, rs_ms):
     # the reduction's blocks are dispatched ahead of the backward's as SMs free
     # up (the backward occupies every SM, as its GEMMs would)
     comm = torch.cuda.Stream(priority=-1)
+    max_ctas = torch.cuda.get_device_properties(G.device).multi_processor_count
 
     def backward_bucket(lo, n):
         for r in range(w.N):
@@ -526,7 +528,8 @@ def run_buckets(args, w, G, T, M, V, W, ws, nrm, cfg, stream, rs_ms):
             ev = torch.cuda.Event()
             ev.record(main)
             comm.wait_event(ev)
-            dpz.dp_reduce_scatter_avg_range(G, w.N, lo, n, ws=ws, stream=comm)
+            dpz.dp_reduce_scatter_avg_range(G, w.N, lo, n, ws=ws, stream=comm,
+                                            max_ctas=max_ctas)
         dpz.dp_grad_norm_finalize(ws, w.P, w.N, nrm, stream=comm)
         dpz.dp_zero1_update(G, T, M, V, W, w.N, cfg, ws=ws, stream=comm)
         main.wait_stream(comm)
@@ -551,7 +554,7 @@ def run_buckets(args, w, G, T, M, V, W, ws, nrm, cfg, stream, rs_ms):
     t_over = timed(overlapped)
     # only the reduce-scatter can run before the last bucket exists; the norm
     # and the update need every bucket
-    return {"buckets": len(buckets), "backward_ms": round(t_back, 3),
+    return {"buckets": len(buckets), "max_ctas": max_ctas, "backward_ms": round(t_back, 3),
             "serial_ms": round(t_serial, 3), "overlapped_ms": round(t_over, 3),
             "reduce_scatter_ms": round(rs_ms, 3),
             "reduce_scatter_hidden_fraction": round((t_serial - t_over) / rs_ms, 3)}

@@ -352,10 +352,17 @@ static int check_range(int64_t P, int N, int64_t lo, int64_t n, bool segment_ali
     return DPZ_OK;
 }
 
+static int check_max_ctas(int max_ctas)
+{
+    if (max_ctas < 0) return fail(DPZ_ERR_INVALID_ARG, "max_ctas = %d is negative", max_ctas);
+    return DPZ_OK;
+}
+
 DPZ_API int dp_reduce_scatter_avg_range(void* grads, int64_t P, int N, int gdtype, int64_t lo,
-                                        int64_t n, void* ws, void* stream)
+                                        int64_t n, void* ws, int max_ctas, void* stream)
 {
     DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_max_ctas(max_ctas));
     DPZ_TRY(check_dtype(gdtype, "gradient", true));
     DPZ_TRY(check_ptr(grads, "grads", gdtype));
     DPZ_TRY(check_range(P, N, lo, n, ws != nullptr));
@@ -367,16 +374,18 @@ DPZ_API int dp_reduce_scatter_avg_range(void* grads, int64_t P, int N, int gdtyp
     const Arena a = make_arena(P, N, gdtype, gdtype);
     const Avg avg = make_avg(N);
     const int es = elem_bytes(gdtype);
-    const RangeArgs g{static_cast<char*>(grads) + lo * es, P, grads, P, lo, lo + n};
+    const RangeArgs g{static_cast<char*>(grads) + lo * es, P, grads, P, lo, lo + n, max_ctas};
     cudaStream_t s = as_stream(stream);
     DPZ_TRY(launch(s, [&] { return launch_reduce_range(a, avg, g, ws, s); }));
     return ok();
 }
 
 DPZ_API int dp_reduce_scatter_avg_bucket(const void* staging, int64_t lo, int64_t n, void* shards,
-                                         int64_t P, int N, int gdtype, void* ws, void* stream)
+                                         int64_t P, int N, int gdtype, void* ws, int max_ctas,
+                                         void* stream)
 {
     DPZ_TRY(check_dims(P, N));
+    DPZ_TRY(check_max_ctas(max_ctas));
     DPZ_TRY(check_dtype(gdtype, "gradient", true));
     DPZ_TRY(check_ptr(staging, "staging", gdtype));
     DPZ_TRY(check_ptr(shards, "shards", gdtype));
@@ -391,7 +400,7 @@ DPZ_API int dp_reduce_scatter_avg_bucket(const void* staging, int64_t lo, int64_
     DPZ_TRY(check_disjoint(rs));
     const Arena a = make_arena(P, N, gdtype, gdtype);
     const Avg avg = make_avg(N);
-    const RangeArgs g{staging, n, shards, 0, lo, lo + n};
+    const RangeArgs g{staging, n, shards, 0, lo, lo + n, max_ctas};
     cudaStream_t s = as_stream(stream);
     DPZ_TRY(launch(s, [&] { return launch_reduce_range(a, avg, g, ws, s); }));
     return ok();

@@ -83,12 +83,15 @@ cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaS
 // A range [lo, hi) of arena elements to reduce: rank r's value of element e
 // at src + r*src_stride + (e - lo), the average of element e (chunk c) stored
 // at dst + c*dst_stride + e (strides and offsets in elements).
+// max_ctas > 0 caps the blocks of the launch (each then loops over its part
+// of the range); 0: one pass.
 struct RangeArgs {
     const void* src;
     int64_t src_stride;
     void* dst;
     int64_t dst_stride;
     int64_t lo, hi;
+    int max_ctas;
 };
 cudaError_t launch_reduce_range(const Arena& a, const Avg& avg, const RangeArgs& g, void* ws,
                                 cudaStream_t s);

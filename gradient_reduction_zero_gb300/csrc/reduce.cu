@@ -92,10 +92,12 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
 // arena, dst_stride = P.  From a staging bucket into compact shards (ZeRO-2):
 // src = staging [N][hi - lo], src_stride = hi - lo, dst = shards [P],
 // dst_stride = 0.  Block row y takes the part of the range inside chunk
-// c_first + y, one 32-group run per warp, one-shot.  With SUMSQ the range
-// must start and end on 256-element segment boundaries of its chunks; the
-// runs are then the segments and their partials are the ones the
-// whole-arena kernels write.
+// c_first + y in 32-group runs, one per warp: one pass when the grid covers
+// the piece, else each warp loops with the grid's stride (a capped grid that
+// leaves SMs to kernels on other streams).  With SUMSQ the range must start
+// and end on 256-element segment boundaries of its chunks; the runs are then
+// the segments and their partials are the ones the whole-arena kernels
+// write.
 template <int GDT, int NT, bool SUMSQ>
 __global__ void __launch_bounds__(kBlock)
 k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restrict__ dst,
@@ -113,34 +115,36 @@ k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restric
     const int64_t plo = lo > c * C ? lo : c * C;
     const int64_t phi = hi < (c + 1) * C ? hi : (c + 1) * C;
     const int64_t groups = (phi - plo) / kGroup;
-    const int64_t wp = global_warp();                     // run of the piece
-    if (plo >= phi || wp * 32 >= groups) return;          // whole warps
+    if (plo >= phi) return;
     const int64_t seg0 = (plo - c * C) / kSegment;        // first segment of the piece
-    const int64_t gi = wp * 32 + lane;
-    float ss = 0.0f;
-    if (gi < groups) {
-        const int64_t e = plo + gi * kGroup;
-        const int64_t soff = (e - lo) * ES;
-        float acc[8];
-        if constexpr (NT > 0) {
-            typename G::Raw raw[NT];
+    const int64_t wstride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t wp = global_warp(); wp * 32 < groups; wp += wstride) {   // whole warps
+        const int64_t gi = wp * 32 + lane;
+        float ss = 0.0f;
+        if (gi < groups) {
+            const int64_t e = plo + gi * kGroup;
+            const int64_t soff = (e - lo) * ES;
+            float acc[8];
+            if constexpr (NT > 0) {
+                typename G::Raw raw[NT];
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                int r = c + 1 + j;
-                if (r >= NT) r -= NT;
-                raw[j] = G::load_raw(src + r * sslab + soff);
+                for (int j = 0; j < NT; ++j) {
+                    int r = c + 1 + j;
+                    if (r >= NT) r -= NT;
+                    raw[j] = G::load_raw(src + r * sslab + soff);
+                }
+                fold_loaded<GDT, NT>(raw, acc);
+            } else {
+                ring_fold<GDT>(src, sslab, soff, c, N, acc);
             }
-            fold_loaded<GDT, NT>(raw, acc);
-        } else {
-            ring_fold<GDT>(src, sslab, soff, c, N, acc);
+            average8<GDT>(acc, avg);
+            if (SUMSQ) ss = sumsq8(acc);
+            G::store_raw(dst + (c * dst_stride + e) * ES, G::pack(acc));
         }
-        average8<GDT>(acc, avg);
-        if (SUMSQ) ss = sumsq8(acc);
-        G::store_raw(dst + (c * dst_stride + e) * ES, G::pack(acc));
-    }
-    if (SUMSQ) {
-        const float t = warp_sum_f32(ss);
-        if (lane == 0) partials[c * segs + seg0 + wp] = (double)t;
+        if (SUMSQ) {
+            const float t = warp_sum_f32(ss);
+            if (lane == 0) partials[c * segs + seg0 + wp] = (double)t;
+        }
     }
 }
 
@@ -323,7 +327,11 @@ static cudaError_t range_t(const Arena& a, const Avg& avg, const RangeArgs& g, v
     const int c_last = (int)((g.hi - 1) / a.C);
     const int pieces = c_last - c_first + 1;
     const int64_t longest = a.C < g.hi - g.lo ? a.C : g.hi - g.lo;
-    const dim3 grid(blocks_for_segments(segments_per_chunk(longest), 1), (unsigned)pieces, 1);
+    dim3 grid(blocks_for_segments(segments_per_chunk(longest), 1), (unsigned)pieces, 1);
+    if (g.max_ctas > 0) {
+        const unsigned per_piece = g.max_ctas / pieces > 0 ? (unsigned)(g.max_ctas / pieces) : 1u;
+        if (grid.x > per_piece) grid.x = per_piece;
+    }
     set_last_kernel_name(SUMSQ ? "dpz_rs_range_sumsq" : "dpz_rs_range");
     k_reduce_range<GDT, NT, SUMSQ><<<grid, kBlock, 0, s>>>(
         static_cast<const char*>(g.src), g.src_stride, static_cast<char*>(g.dst), g.dst_stride,

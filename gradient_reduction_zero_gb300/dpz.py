@@ -55,9 +55,11 @@ _SIGS = {
     "dp_grad_global_norm_static": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _FP, _VP],
                                    ctypes.c_int),
     "dp_reduce_scatter_avg_range": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
-                                     ctypes.c_int64, ctypes.c_int64, _VP, _VP], ctypes.c_int),
+                                     ctypes.c_int64, ctypes.c_int64, _VP, ctypes.c_int, _VP],
+                                    ctypes.c_int),
     "dp_reduce_scatter_avg_bucket": ([_VP, ctypes.c_int64, ctypes.c_int64, _VP, ctypes.c_int64,
-                                      ctypes.c_int, ctypes.c_int, _VP, _VP], ctypes.c_int),
+                                      ctypes.c_int, ctypes.c_int, _VP, ctypes.c_int, _VP],
+                                     ctypes.c_int),
     "dp_grad_norm_finalize": ([_VP, ctypes.c_int64, ctypes.c_int, _FP, _VP], ctypes.c_int),
     "dp_zero1_update": ([_VP, _FP, _FP, _FP, _VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                          ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _VP], ctypes.c_int),
@@ -193,18 +195,20 @@ def dp_zero1_step(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None, 
 
 
 def dp_reduce_scatter_avg_range(grads, N: int, lo: int, n: int, ws=None, stream=None,
-                                acc32: bool = False) -> None:
+                                acc32: bool = False, max_ctas: int = 0) -> None:
+    """max_ctas: 0 = one pass over the range; > 0 caps the kernel's blocks
+    (for example one per SM) to leave the GPU to kernels on other streams."""
     _check(lib.dp_reduce_scatter_avg_range(_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32),
-                                           lo, n, _ptr(ws), _stream_handle(stream)))
+                                           lo, n, _ptr(ws), max_ctas, _stream_handle(stream)))
 
 
 def dp_reduce_scatter_avg_bucket(staging, lo: int, shards, N: int, ws=None, stream=None,
-                                 acc32: bool = False) -> None:
+                                 acc32: bool = False, max_ctas: int = 0) -> None:
     """staging: [N*n] (rank r's values of arena elements [lo, lo+n) at r*n);
-    shards: [P]."""
+    shards: [P].  max_ctas as in dp_reduce_scatter_avg_range."""
     n = _np(staging, N)
     _check(lib.dp_reduce_scatter_avg_bucket(_ptr(staging), lo, n, _ptr(shards), shards.numel(),
-                                            N, dtype_code(staging, acc32), _ptr(ws),
+                                            N, dtype_code(staging, acc32), _ptr(ws), max_ctas,
                                             _stream_handle(stream)))
 
 

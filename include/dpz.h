@@ -204,6 +204,16 @@ DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v,
  * chunks ((lo mod C) and ((lo+n) mod C) multiples of 256) and its norm
  * partials are written; once every bucket is reduced, dp_grad_norm_finalize
  * gives the same norm, bit for bit, as the whole-arena calls.
+ *
+ * max_ctas bounds the thread blocks of the reduction kernel.  0: one pass
+ * with as many blocks as the range needs, the fastest when nothing else runs.
+ * > 0: at most max(max_ctas, c) blocks, where c is the number of chunks the
+ * range touches, each looping over its part of the range.  A reduction that
+ * runs beside compute kernels on other streams (a backward pass) should leave
+ * them most of the GPU: with one block per SM it hid about 60 % of its time
+ * behind a compute-bound stand-in on GB300, against about 10 % with 0, whose
+ * blocks take every SM slot that the compute kernels free.  The result is the
+ * same, bit for bit, for every max_ctas.  Negative: DPZ_ERR_INVALID_ARG.
  * ------------------------------------------------------------------- */
 
 /* ZeRO-1 with buckets: reduce + average elements [lo, lo+n) of the arena in
@@ -211,7 +221,8 @@ DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v,
  * dp_reduce_scatter_avg does for the whole arena.  ws may be NULL (no norm
  * partials). */
 DPZ_API int dp_reduce_scatter_avg_range(void* grads, int64_t P, int N, int gdtype,
-                                        int64_t lo, int64_t n, void* ws, void* stream);
+                                        int64_t lo, int64_t n, void* ws, int max_ctas,
+                                        void* stream);
 
 /* ZeRO-2: gradients are sharded too ("Lab 09", §4: stage 2 shards the
  * gradients, 2Ψ + 14Ψ/N bytes per rank; "Distributed training":
@@ -223,7 +234,7 @@ DPZ_API int dp_reduce_scatter_avg_range(void* grads, int64_t P, int N, int gdtyp
  * rank keeps a full gradient replica. */
 DPZ_API int dp_reduce_scatter_avg_bucket(const void* staging, int64_t lo, int64_t n,
                                          void* shards, int64_t P, int N, int gdtype,
-                                         void* ws, void* stream);
+                                         void* ws, int max_ctas, void* stream);
 
 /* The global norm from the partials that the range or bucket calls left in
  * ws (all of [0, P) reduced, with ws); writes it into ws and, if not NULL,

@@ -139,17 +139,21 @@ def test_bucket_calls_reject(dpz):
     L = dpz.lib
     P, N = 4 * 6152, 4            # chunk 6152 = 24 segments of 256 + 8 elements
     ws = A + 512 * MB
-    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, -8, 64, None, None) == 1
-    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, P - 8, 16, None, None) == 1
-    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 4, 64, None, None) == 2      # lo % 8
-    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 0, 12, None, None) == 2      # n % 8
+    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, -8, 64, None, 0, None) == 1
+    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, P - 8, 16, None, 0, None) == 1
+    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 4, 64, None, 0, None) == 2      # lo % 8
+    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 0, 12, None, 0, None) == 2      # n % 8
     # with norm partials the range must sit on segment boundaries of its chunks
-    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 8, 256, ws, None) == 2
-    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 0, 6000, ws, None) == 2
-    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 0, 6152 + 256, A + 16, None) == 1  # overlap
+    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 8, 256, ws, 0, None) == 2
+    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 0, 6000, ws, 0, None) == 2
+    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 0, 6152 + 256, A + 16, 0, None) == 1  # overlap
     # staging and shards must not overlap
-    assert L.dp_reduce_scatter_avg_bucket(A, 0, 256, A + 512, P, N, 1, None, None) == 1
-    assert L.dp_reduce_scatter_avg_bucket(None, 0, 256, A + MB, P, N, 1, None, None) == 1
+    assert L.dp_reduce_scatter_avg_bucket(A, 0, 256, A + 512, P, N, 1, None, 0, None) == 1
+    assert L.dp_reduce_scatter_avg_bucket(None, 0, 256, A + MB, P, N, 1, None, 0, None) == 1
+    # a negative block cap
+    assert L.dp_reduce_scatter_avg_range(A, P, N, 1, 0, 64, None, -1, None) == 1
+    assert b"max_ctas" in L.dpz_last_error()
+    assert L.dp_reduce_scatter_avg_bucket(A, 0, 256, A + MB, P, N, 1, None, -1, None) == 1
     assert L.dp_grad_norm_finalize(None, P, N, None, None) == 1
     cfg = _cfg(dpz, clip=1.0)
     assert L.dp_zero2_update(A, A + MB, A + 2 * MB, A + 3 * MB, A + 4 * MB, P, N, 1, 1,

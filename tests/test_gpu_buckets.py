@@ -57,7 +57,10 @@ def fused_reference(w, g, th, m, v, acc32):
 @pytest.mark.parametrize("N,C,nb", [(4, 6152, 7), (8, 2056, 5), (3, 1000, 4), (4, 262_144, 12)])
 @pytest.mark.parametrize("clip", [0.0, 1e-3])
 @pytest.mark.parametrize("acc32", [False, True])
-def test_bucketed_zero1_matches_whole_arena(N, C, nb, clip, acc32):
+@pytest.mark.parametrize("max_ctas", [0, 1, 152])
+def test_bucketed_zero1_matches_whole_arena(N, C, nb, clip, acc32, max_ctas):
+    """max_ctas = 1: one block per chunk piece loops over the whole piece;
+    152: one block per SM; 0: one pass."""
     w, g, th, m, v = problem(N, C, clip, seed=N + nb)
     ref = fused_reference(w, g, th, m, v, acc32)
     P = w.P
@@ -75,7 +78,8 @@ def test_bucketed_zero1_matches_whole_arena(N, C, nb, clip, acc32):
         ev = torch.cuda.Event()
         ev.record(main)
         comm.wait_event(ev)                                 # never reduce before it exists
-        dpz.dp_reduce_scatter_avg_range(G, N, lo, n, ws=ws, stream=comm, acc32=acc32)
+        dpz.dp_reduce_scatter_avg_range(G, N, lo, n, ws=ws, stream=comm, acc32=acc32,
+                                        max_ctas=max_ctas)
     dpz.dp_grad_norm_finalize(ws, P, N, nrm, stream=comm)
     dpz.dp_zero1_update(G, T, M, V, W, N, cfg, ws=ws, stream=comm)
     main.wait_stream(comm)
@@ -92,7 +96,8 @@ def test_bucketed_zero1_matches_whole_arena(N, C, nb, clip, acc32):
 @pytest.mark.parametrize("N,C,nb", [(4, 6152, 7), (8, 2056, 5), (3, 1000, 4), (4, 262_144, 12)])
 @pytest.mark.parametrize("clip", [0.0, 1e-3])
 @pytest.mark.parametrize("acc32", [False, True])
-def test_zero2_matches_zero1(N, C, nb, clip, acc32):
+@pytest.mark.parametrize("max_ctas", [0, 2])
+def test_zero2_matches_zero1(N, C, nb, clip, acc32, max_ctas):
     w, g, th, m, v = problem(N, C, clip, seed=2 * N + nb)
     ref = fused_reference(w, g, th, m, v, acc32)
     P = w.P
@@ -117,7 +122,8 @@ def test_zero2_matches_zero1(N, C, nb, clip, acc32):
         ready = torch.cuda.Event()
         ready.record(main)
         comm.wait_event(ready)
-        dpz.dp_reduce_scatter_avg_bucket(stage, lo, shards, N, ws=ws, stream=comm, acc32=acc32)
+        dpz.dp_reduce_scatter_avg_bucket(stage, lo, shards, N, ws=ws, stream=comm, acc32=acc32,
+                                         max_ctas=max_ctas)
         done = torch.cuda.Event()
         done.record(comm)
     dpz.dp_grad_norm_finalize(ws, P, N, nrm, stream=comm)
