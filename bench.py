@@ -647,7 +647,9 @@ def run_e2e(args, w, G, step, nrm, stream, world, full=None):
            "how": (f"pinned host gradients, {len(buckets)} buckets copied on one stream and "
                    "reduced on another (dp_reduce_scatter_avg_range, events), then "
                    "dp_grad_norm_finalize + dp_zero1_update; norm read back")
-           if use_pipe else "pinned host gradients copied, dp_zero1_step, norm read back",
+           if use_pipe else ("pinned host gradients copied, dp_allreduce_avg, one element read "
+                             "back" if w.allreduce_only else
+                             "pinned host gradients copied, dp_zero1_step, norm read back"),
            "plain_ms_per_step": round(dt_plain * 1e3, 3)}
     return out
 
