@@ -236,6 +236,50 @@ def time_oracle(w: I.Workload, seconds: float) -> dict:
                       f"of {w.name} ({elapsed:.1f} s single-threaded)"}
 
 
+def time_oracle_threads(w: I.Workload, seconds: float, threads: int) -> dict:
+    """The same oracle, unchanged, on `threads` disjoint windows of the
+    workload at once, one host thread each (the oracle's C calls release the
+    GIL), for about `seconds` of wall time; throughput in the metric's unit."""
+    import threading
+    import oracle as O
+    width = min(w.C, 1 << 18)
+    cfg = O.cfg_from_workload(w)
+    mini = w.with_(P=w.N * width)
+    span = max(1, (w.C - width) // max(1, threads))
+    bases = [oracle_window_step(w, width, offset=min(w.C - width, t * span) // 8 * 8)
+             for t in range(threads)]
+    counts = [0] * threads
+    start = threading.Barrier(threads + 1)
+    stop = threading.Event()
+
+    def work(t):
+        start.wait()
+        while not stop.is_set() or counts[t] == 0:
+            args = [a.copy() for a in bases[t]]
+            if w.allreduce_only:
+                O.ring_allreduce_avg(args[0])
+            else:
+                O.zero1_step(*args, cfg)
+            counts[t] += 1
+
+    pool = [threading.Thread(target=work, args=(t,)) for t in range(threads)]
+    for th in pool:
+        th.start()
+    start.wait()
+    t0 = time.perf_counter()
+    time.sleep(seconds)
+    stop.set()
+    for th in pool:
+        th.join()
+    elapsed = time.perf_counter() - t0
+    done = sum(counts)
+    return {"value": done * step_bytes(mini) / elapsed / 1e9, "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"{done} windows of {width} elements per chunk x {w.N} chunks x {w.N} ranks "
+                      f"of {w.name} on {threads} host threads, disjoint windows "
+                      f"({elapsed:.1f} s wall)"}
+
+
 def run_reference(args) -> None:
     """The CPU oracle timed as the reference arm: rank 0 only, each step a
     bounded window of the workload, the whole run kept to a few minutes."""
@@ -439,9 +483,10 @@ def run_gpu(args) -> None:
         full = None if w.allreduce_only or w.clip <= 0 else (T, M, V, W, ws, cfg)
         e2e = run_e2e(args, w, G, step, nrm, stream, world, full)
 
-    cpu = None
+    cpu = cpu_mt = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = time_oracle(w, args.cpu_seconds)
+        cpu_mt = time_oracle_threads(w, args.cpu_seconds, os.cpu_count() or 1)
 
     if rank == 0:
         line = {
@@ -466,6 +511,7 @@ def run_gpu(args) -> None:
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "cpu_baseline_threads": cpu_mt,
         }
         if graph is not None:
             line["graph_replay"] = graph

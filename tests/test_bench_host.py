@@ -76,3 +76,12 @@ def test_reference_arm_nonzero_rank_does_nothing():
                           "--workload", I.TINY.name, "--steps", "1", "--warmup", "0"],
                          capture_output=True, text=True, timeout=120, env=env)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_cpu_baselines_single_and_threaded():
+    """The oracle timed on one thread and on several disjoint windows at once."""
+    one = bench.time_oracle(I.GPT2_124M, 0.2)
+    many = bench.time_oracle_threads(I.GPT2_124M, 0.2, 2)
+    for r, cores in ((one, 1), (many, 2)):
+        assert r["kind"] == "oracle" and r["unit"] == bench.UNIT and r["cores"] == cores
+        assert r["value"] > 0 and "windows" in r["sample"]
