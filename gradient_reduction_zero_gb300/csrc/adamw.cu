@@ -149,30 +149,6 @@ static cudaError_t fused_n(const Arena& a, const Avg& avg, const AdamArgs& h, bo
 }
 
 template <int GDT, int WDT>
-static cudaError_t bcast_n(const Arena& a, const Avg& avg, const AdamArgs& h, void* grads,
-                           float* master, float* m, float* v, void* weights, void* ws,
-                           cudaStream_t s, int64_t avg_stride)
-{
-    switch (a.N) {
-    case 1:
-        return adamw_t<GDT, WDT, 1, false, true, false>(a, avg, h, false, grads, master, m, v,
-                                                        weights, ws, s, avg_stride);
-    case 2:
-        return adamw_t<GDT, WDT, 2, false, true, false>(a, avg, h, false, grads, master, m, v,
-                                                        weights, ws, s, avg_stride);
-    case 4:
-        return adamw_t<GDT, WDT, 4, false, true, false>(a, avg, h, false, grads, master, m, v,
-                                                        weights, ws, s, avg_stride);
-    case 8:
-        return adamw_t<GDT, WDT, 8, false, true, false>(a, avg, h, false, grads, master, m, v,
-                                                        weights, ws, s, avg_stride);
-    default:
-        return adamw_t<GDT, WDT, 0, false, true, false>(a, avg, h, false, grads, master, m, v,
-                                                        weights, ws, s, avg_stride);
-    }
-}
-
-template <int GDT, int WDT>
 static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                             bool bcast, bool store_avg, void* grads, float* master, float* m,
                             float* v, void* weights, void* ws, cudaStream_t s,
@@ -185,8 +161,8 @@ static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, A
         return fused_n<GDT, WDT, false>(a, avg, h, store_avg, grads, master, m, v, weights, ws,
                                         s);
     }
-    if (bcast)
-        return bcast_n<GDT, WDT>(a, avg, h, grads, master, m, v, weights, ws, s, avg_stride);
+    if (bcast)      // staged through shared memory by bulk copies (adamw_tma.cu)
+        return launch_adamw_bcast_tma(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     return adamw_t<GDT, WDT, 0, false, false, false>(a, avg, h, false, grads, master, m, v,
                                                     weights, ws, s, avg_stride);
 }

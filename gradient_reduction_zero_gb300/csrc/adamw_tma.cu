@@ -1,0 +1,265 @@
+// AdamW + cast + all-gather of the new weights from the stored averages,
+// staged through shared memory by the Blackwell bulk-copy engine (TMA, 1-D
+// cp.async.bulk).
+//
+// One-shot grid of 128-thread CTAs, one 1024-element tile each, in the
+// chunk-major order of the other streaming kernels.  Thread 0 issues the bulk
+// loads of the tile's averaged gradient and master/m/v into shared memory,
+// completing on one mbarrier; every thread updates 8 elements in shared
+// memory; thread 0 then bulk-stores master/m/v and the cast weights into the
+// N weight slabs and waits until those stores have read shared memory.  The
+// arithmetic is adamw_elem, so the results are bit-identical to k_adamw.
+//
+// The wait on the mbarrier is bounded by the SM clock: if the tile has not
+// arrived after about two seconds the CTA sets the device error flag that
+// dpz_device_status reads, waits (again bounded) for its loads in flight, and
+// returns without storing.
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace dpz {
+
+constexpr int kTmaTile = 1024;                     // elements per CTA
+constexpr int kTmaThreads = kTmaTile / kGroup;     // 128: 8 elements each
+constexpr long long kWaitLimitCycles = 4000000000LL;
+
+__device__ unsigned g_pipeline_error;
+
+template <int GDT, int WDT>
+struct TmaTile {
+    unsigned char avg[kTmaTile * Group<GDT>::kBytes];
+    float th[kTmaTile];
+    float m[kTmaTile];
+    float v[kTmaTile];
+    unsigned char w[kTmaTile * Group<WDT>::kBytes];
+};
+
+namespace {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// global -> shared, completing `bytes` on the mbarrier
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_addr(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// shared -> global, in the current bulk group
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_addr(ssrc)), "r"(bytes)
+                 : "memory");
+}
+
+}  // namespace
+
+// grads: the averaged gradient of element e (chunk c) at grads + (c*avg_stride
+// + e) elements; hdr: the workspace header (the norm), read when clip > 0.
+// NT > 0: N == NT known at compile time; NT == 0: any N, read from n_rt.
+template <int GDT, int WDT, int NT>
+__global__ void __launch_bounds__(kTmaThreads)
+k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __restrict__ master,
+                  float* __restrict__ mom, float* __restrict__ var, char* __restrict__ weights,
+                  int64_t P, int64_t C, int n_rt, AdamArgs h, const WsHeader* __restrict__ hdr)
+{
+    using GS = Group<GDT>;
+    using WS = Group<WDT>;
+    constexpr int GES = GS::kBytes;
+    constexpr int WES = WS::kBytes;
+    const int N = NT > 0 ? NT : n_rt;
+    extern __shared__ __align__(128) unsigned char dsmem[];
+    TmaTile<GDT, WDT>& t = *reinterpret_cast<TmaTile<GDT, WDT>*>(dsmem);
+    __shared__ __align__(8) uint64_t full;
+    __shared__ int timed_out;
+
+    // tile b of the chunk-major tile list: chunk c, first element e, n elements
+    const int64_t tiles_per_chunk = (C + kTmaTile - 1) / kTmaTile;
+    const int c = (int)(blockIdx.x / tiles_per_chunk);
+    const int64_t tc = blockIdx.x - (int64_t)c * tiles_per_chunk;
+    const int64_t e = (int64_t)c * C + tc * kTmaTile;
+    const int64_t left = C - tc * kTmaTile;
+    const int n = (int)(left < kTmaTile ? left : kTmaTile);   // a multiple of 8
+    const int tid = threadIdx.x;
+
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&full)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        timed_out = 0;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                         smem_addr(&full)),
+                     "r"((uint32_t)n * (GES + 12u))
+                     : "memory");
+        bulk_load(t.avg, grads + ((int64_t)c * avg_stride + e) * GES, (uint32_t)n * GES, &full);
+        bulk_load(t.th, master + e, (uint32_t)n * 4u, &full);
+        bulk_load(t.m, mom + e, (uint32_t)n * 4u, &full);
+        bulk_load(t.v, var + e, (uint32_t)n * 4u, &full);
+    }
+    __syncthreads();     // the barrier is initialised before anyone waits on it
+
+    float scale = 1.0f;
+    bool do_scale = false;
+    if (h.clip > 0.0f) {
+        const float nrm = hdr->norm;
+        if (nrm > h.clip) {
+            scale = __fdiv_rn(h.clip, nrm);
+            do_scale = true;
+        }
+    }
+
+    if (!mbar_try_wait(&full, 0)) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&full, 0)) {
+            if (clock64() - t0 > kWaitLimitCycles) {
+                atomicExch(&timed_out, 1);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    if (timed_out) {
+        if (tid == 0) {
+            atomicExch(&g_pipeline_error, 1u);
+            // the loads may still land: shared memory must outlive them
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&full, 0) && clock64() - t0 < kWaitLimitCycles) {
+            }
+        }
+        return;
+    }
+
+    const int i0 = tid * kGroup;
+    if (i0 < n) {
+        float g[8], th[8], mm[8], vv[8];
+        GS::unpack(*reinterpret_cast<const typename GS::Raw*>(t.avg + i0 * GES), g);
+        Group<0>::unpack(*reinterpret_cast<const U8*>(&t.th[i0]), th);
+        Group<0>::unpack(*reinterpret_cast<const U8*>(&t.m[i0]), mm);
+        Group<0>::unpack(*reinterpret_cast<const U8*>(&t.v[i0]), vv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float gq = do_scale ? __fmul_rn(g[q], scale) : g[q];
+            adamw_elem(th[q], mm[q], vv[q], gq, h);
+        }
+        *reinterpret_cast<U8*>(&t.th[i0]) = Group<0>::pack(th);
+        *reinterpret_cast<U8*>(&t.m[i0]) = Group<0>::pack(mm);
+        *reinterpret_cast<U8*>(&t.v[i0]) = Group<0>::pack(vv);
+        *reinterpret_cast<typename WS::Raw*>(t.w + i0 * WES) = WS::pack(th);
+    }
+    // the threads' shared-memory writes become visible to the bulk stores
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(master + e, t.th, (uint32_t)n * 4u);
+        bulk_store(mom + e, t.m, (uint32_t)n * 4u);
+        bulk_store(var + e, t.v, (uint32_t)n * 4u);
+        if constexpr (NT > 0) {
+#pragma unroll
+            for (int r = 0; r < NT; ++r)
+                bulk_store(weights + ((int64_t)r * P + e) * WES, t.w, (uint32_t)n * WES);
+        } else {
+            for (int r = 0; r < N; ++r)
+                bulk_store(weights + ((int64_t)r * P + e) * WES, t.w, (uint32_t)n * WES);
+        }
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        // shared memory is released when the CTA exits: wait until the stores
+        // have read it (their writes to global memory complete on their own)
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    }
+}
+
+namespace {
+
+std::mutex g_attr_mu;
+std::map<std::pair<int, const void*>, bool> g_attr_set;   // (device, kernel) done
+
+// Raise the kernel's dynamic shared memory limit on the current device, once.
+cudaError_t allow_smem(const void* fn, size_t smem)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (g_attr_set.count({dev, fn})) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) g_attr_set[{dev, fn}] = true;
+    return e;
+}
+
+template <int GDT, int WDT, int NT>
+cudaError_t tma_t(const Arena& a, const AdamArgs& h, const void* grads, int64_t avg_stride,
+                  float* master, float* m, float* v, void* weights, const void* ws,
+                  cudaStream_t s)
+{
+    auto fn = k_adamw_bcast_tma<GDT, WDT, NT>;
+    const size_t smem = sizeof(TmaTile<GDT, WDT>);
+    const cudaError_t e = allow_smem(reinterpret_cast<const void*>(fn), smem);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (a.C + kTmaTile - 1) / kTmaTile * a.N;
+    set_last_kernel_name("dpz_adamw_bcast");
+    fn<<<(unsigned)tiles, kTmaThreads, smem, s>>>(static_cast<const char*>(grads), avg_stride,
+                                                  master, m, v, static_cast<char*>(weights), a.P,
+                                                  a.C, a.N, h,
+                                                  static_cast<const WsHeader*>(ws));
+    return cudaGetLastError();
+}
+
+template <int GDT, int WDT>
+cudaError_t tma_n(const Arena& a, const AdamArgs& h, const void* grads, int64_t avg_stride,
+                  float* master, float* m, float* v, void* weights, const void* ws,
+                  cudaStream_t s)
+{
+    switch (a.N) {
+    case 1: return tma_t<GDT, WDT, 1>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    case 2: return tma_t<GDT, WDT, 2>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    case 4: return tma_t<GDT, WDT, 4>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    case 8: return tma_t<GDT, WDT, 8>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    default: return tma_t<GDT, WDT, 0>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
+                                   int64_t avg_stride, float* master, float* m, float* v,
+                                   void* weights, const void* ws, cudaStream_t s)
+{
+    const bool gbf = a.gdt != 0;       // stored averages: bf16 in both bf16 modes
+    if (gbf && a.wdt == 1) return tma_n<1, 1>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    if (gbf) return tma_n<1, 0>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    if (a.wdt == 1) return tma_n<0, 1>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    return tma_n<0, 0>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+}
+
+cudaError_t read_and_clear_pipeline_error(unsigned* flag)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flag, g_pipeline_error, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_pipeline_error, &zero, sizeof(unsigned));
+}
+
+}  // namespace dpz

@@ -203,6 +203,18 @@ DPZ_API const char* dpz_version(void) { return "dpz 0.1 (sm_103a)"; }
 
 DPZ_API int64_t dpz_launch_count(void) { return g_launches.load(); }
 
+DPZ_API int dpz_device_status(int* flag_out)
+{
+    if (flag_out == nullptr) return fail(DPZ_ERR_INVALID_ARG, "flag_out is NULL");
+    unsigned f = 0;
+    const cudaError_t e = read_and_clear_pipeline_error(&f);
+    if (e != cudaSuccess)
+        return fail(DPZ_ERR_CUDA, "reading the device error flag failed: %s",
+                    cudaGetErrorString(e));
+    *flag_out = f != 0;
+    return ok();
+}
+
 DPZ_API int dp_reduce_scatter_avg(void* grads, int64_t P, int N, int gdtype, void* stream)
 {
     DPZ_TRY(check_dims(P, N));

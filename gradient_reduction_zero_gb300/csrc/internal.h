@@ -102,6 +102,15 @@ cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, Adam
                          int64_t avg_stride);
 cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 
+// AdamW + cast + all-gather from the stored averages (element e of chunk c
+// at grads + c*avg_stride + e), staged through shared memory by bulk copies
+// (adamw_tma.cu).  A tile that does not arrive within the wait limit sets the
+// device error flag that read_and_clear_pipeline_error returns.
+cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
+                                   int64_t avg_stride, float* master, float* m, float* v,
+                                   void* weights, const void* ws, cudaStream_t s);
+cudaError_t read_and_clear_pipeline_error(unsigned* flag);
+
 
 // The fixed device scratch of dp_grad_global_norm_static (norm_static.cu):
 // its size in bytes, and its device address on the current device (looked

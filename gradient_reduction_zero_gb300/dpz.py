@@ -68,6 +68,7 @@ _SIGS = {
     "dpz_last_error": ([], ctypes.c_char_p),
     "dpz_version": ([], ctypes.c_char_p),
     "dpz_launch_count": ([], ctypes.c_int64),
+    "dpz_device_status": ([ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "dpz_profile_start": ([ctypes.c_int], ctypes.c_int),
     "dpz_profile_stop": ([ctypes.POINTER(KernelStat), ctypes.c_int,
                           ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
@@ -232,6 +233,14 @@ def dp_zero2_update(shards, master, m, v, weights, N: int, cfg: AdamWCfg, ws=Non
 
 def launch_count() -> int:
     return int(lib.dpz_launch_count())
+
+
+def device_status() -> int:
+    """The device error flag (1 if a kernel's bounded wait on its own copies
+    ran out since the last call), read and cleared."""
+    f = ctypes.c_int()
+    _check(lib.dpz_device_status(ctypes.byref(f)))
+    return f.value
 
 
 def version() -> str:

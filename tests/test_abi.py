@@ -161,3 +161,7 @@ def test_bucket_calls_reject(dpz):
     assert L.dp_zero1_update(A, A + MB + 16, A + 2 * MB, A + 3 * MB, A + 4 * MB, P, N, 1, 1,
                              ctypes.byref(_cfg(dpz)), None, None) == 2
 
+
+def test_device_status_rejects_null(dpz):
+    assert dpz.lib.dpz_device_status(None) == 1
+    assert b"flag_out" in dpz.lib.dpz_last_error()

@@ -190,6 +190,23 @@ def test_no_clip_variants(store_avg, want_norm):
     check_step(w, g, th, m, v, wts, out, check_avg=store_avg)
 
 
+@pytest.mark.parametrize("gdt,wdt", [("bf16", "bf16"), ("f32", "f32"), ("bf16", "f32")])
+@pytest.mark.parametrize("N,C", [(4, 3_000_016), (3, 1000), (16, 520)])
+def test_staged_update_equals_owner_update_plus_allgather(gdt, wdt, N, C):
+    """The clipped step's AdamW + all-gather kernel stages 1024-element tiles
+    through shared memory by bulk copies (ragged last tile per chunk, runtime
+    and compile-time N): bit-identical to the owner-only update plus the
+    separate all-gather, and no bounded wait ran out."""
+    w, g, th, m, v, wts = make_problem(N, C, gdt, wdt, 1e-3, seed=17 + N)
+    assert dpz.device_status() == 0
+    a = run_gpu_step(w, g, th, m, v, wts, fused=True)
+    b = run_gpu_step(w, g, th, m, v, wts, fused=False)
+    for x, y in zip(a[:5], b[:5]):
+        assert same_bits(x, y)
+    assert dpz.device_status() == 0
+    check_step(w, g, th, m, v, wts, a)
+
+
 def test_deterministic():
     w, g, th, m, v, wts = make_problem(8, 12344, "bf16", "bf16", 1e-3, seed=1)
     a = run_gpu_step(w, g, th, m, v, wts)
