@@ -41,7 +41,7 @@ UNIT = "GB/s"
 DEFAULT_WORKLOAD = I.GPT2_1P5B.name
 PROFILES = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "gradient_reduction_zero_gb300", "csrc", f)
-                  for f in ("device.cuh", "reduce.cu", "adamw.cu", "adamw_tma.cu", "internal.h")]
+                  for f in ("device.cuh", "bulk.cuh", "reduce.cu", "adamw.cu", "staged.cu", "internal.h")]
 
 
 # ------------------------------------------------------------------ bytes

@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdpz.so")
 
-SOURCES = ["api.cpp", "reduce.cu", "adamw.cu", "adamw_tma.cu", "norm_static.cu"]
+SOURCES = ["api.cpp", "reduce.cu", "adamw.cu", "staged.cu", "norm_static.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("internal.h", "device.cuh")] + \
     [os.path.join(INCLUDE, "dpz.h")]
 

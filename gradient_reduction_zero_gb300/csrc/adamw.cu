@@ -161,7 +161,7 @@ static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, A
         return fused_n<GDT, WDT, false>(a, avg, h, store_avg, grads, master, m, v, weights, ws,
                                         s);
     }
-    if (bcast)      // staged through shared memory by bulk copies (adamw_tma.cu)
+    if (bcast)      // staged through shared memory by bulk copies (staged.cu)
         return launch_adamw_bcast_tma(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     return adamw_t<GDT, WDT, 0, false, false, false>(a, avg, h, false, grads, master, m, v,
                                                     weights, ws, s, avg_stride);

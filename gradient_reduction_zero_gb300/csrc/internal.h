@@ -104,8 +104,9 @@ cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 
 // AdamW + cast + all-gather from the stored averages (element e of chunk c
 // at grads + c*avg_stride + e), staged through shared memory by bulk copies
-// (adamw_tma.cu).  A tile that does not arrive within the wait limit sets the
-// device error flag that read_and_clear_pipeline_error returns.
+// (staged.cu, as is launch_norm_owned).  A tile that does not arrive within
+// the wait limit sets the device error flag that
+// read_and_clear_pipeline_error returns.
 cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
                                    int64_t avg_stride, float* master, float* m, float* v,
                                    void* weights, const void* ws, cudaStream_t s);

@@ -1,6 +1,7 @@
 // Reduce-side kernels: ring-order reduce-scatter + average (optionally with
-// norm partials, optionally written back into every slab = all-reduce),
-// the norm of the owner chunks, its finalisation, and the all-gather.
+// norm partials, optionally written back into every slab = all-reduce), the
+// finalisation of the norm, and the all-gather.  (The standalone norm of the
+// owner chunks is staged through shared memory: staged.cu.)
 //
 // All streaming kernels run one-shot grids over the chunk-major list of
 // 256-element segments (device.cuh): every thread of a warp works on the
@@ -148,56 +149,12 @@ k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restric
     }
 }
 
-// Segments per warp for the single-stream kernels (norm of the owner chunks,
-// all-gather): one 16- or 32-byte load per lane and segment, so several
-// segments keep enough bytes in flight.
+// Segments per warp for the all-gather: one 16- or 32-byte load per lane and
+// segment, so several segments keep enough bytes in flight.
 template <int DT>
 struct StreamSegs {
     static constexpr int value = DT == 0 ? 2 : 4;
 };
-
-// Sums of squares of the owner chunks (chunk c of slab c), per segment.
-template <int GDT>
-__global__ void __launch_bounds__(kBlock)
-k_norm_owned(const char* __restrict__ grads, int64_t P, int64_t C, int N,
-             WsHeader* __restrict__ hdr, double* __restrict__ partials)
-{
-    constexpr int ES = Group<GDT>::kBytes;
-    constexpr int U = StreamSegs<GDT>::value;
-    const int64_t slab = P * ES;
-    const int64_t groups = C / kGroup;
-    const int64_t segs = segments_per_chunk(C);
-    const int64_t total = (int64_t)N * segs;
-    const int lane = threadIdx.x & 31;
-    if (blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
-    const int64_t sw0 = global_warp() * U;
-    if (sw0 >= total) return;                             // whole warps
-    const SegPos p0 = seg_pos(sw0, segs);
-    typename Group<GDT>::Raw raw[U];
-    SegPos p = p0;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int64_t gi = p.seg * 32 + lane;
-        if (sw0 + u < total && gi < groups)
-            raw[u] = Group<GDT>::load_raw(grads + p.c * slab + (p.c * C + gi * kGroup) * ES);
-        seg_next(p, segs);
-    }
-    p = p0;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        if (sw0 + u < total) {
-            float ss = 0.0f;
-            if (p.seg * 32 + lane < groups) {
-                float x[8];
-                Group<GDT>::unpack(raw[u], x);
-                ss = sumsq8(x);
-            }
-            const float t = warp_sum_f32(ss);
-            if (lane == 0) partials[p.c * segs + p.seg] = (double)t;
-        }
-        seg_next(p, segs);
-    }
-}
 
 // Sum of the n segment partials in a fixed order, independent of the device:
 // block b of F adds the contiguous range [b*L, (b+1)*L) (L = ceil(n/F)) into
@@ -363,21 +320,6 @@ cudaError_t launch_reduce_range(const Arena& a, const Avg& avg, const RangeArgs&
     default:
         return sumsq ? range_n<2, true>(a, avg, g, ws, s) : range_n<2, false>(a, avg, g, ws, s);
     }
-}
-
-cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaStream_t s)
-{
-    set_last_kernel_name("dpz_norm_owned");
-    const char* g = static_cast<const char*>(grads);
-    WsHeader* hdr = static_cast<WsHeader*>(ws);
-    const int64_t nseg = int64_t(a.N) * segments_per_chunk(a.C);
-    if (a.gdt != 0)       // both bf16 modes store bf16 averages
-        k_norm_owned<1><<<blocks_for_segments(nseg, StreamSegs<1>::value), kBlock, 0, s>>>(
-            g, a.P, a.C, a.N, hdr, ws_partials(ws));
-    else
-        k_norm_owned<0><<<blocks_for_segments(nseg, StreamSegs<0>::value), kBlock, 0, s>>>(
-            g, a.P, a.C, a.N, hdr, ws_partials(ws));
-    return cudaGetLastError();
 }
 
 cudaError_t launch_norm_finalize(const Arena& a, void* ws, float* norm_out, cudaStream_t s)

@@ -282,13 +282,14 @@ DPZ_API const char* dpz_last_error(void);
 /* Library version string. */
 DPZ_API const char* dpz_version(void);
 
-/* Device-side error flag of the current device, read and cleared.  The
- * AdamW + all-gather kernel that reads stored averages (dp_zero1_step with
- * clipping, dp_zero1_update, dp_zero2_update) stages its tiles through shared
- * memory with asynchronous bulk copies and waits for them on a barrier.  That
- * wait is bounded by the SM clock (about two seconds); if it runs out, the
- * tile is left un-updated and this flag is set, instead of the kernel
- * hanging.  *flag_out = 1 if that happened since the last call, else 0.
+/* Device-side error flag of the current device, read and cleared.  Two
+ * kernels stage their tiles through shared memory with asynchronous bulk
+ * copies and wait for them on a barrier: the AdamW + all-gather kernel that
+ * reads stored averages (dp_zero1_step with clipping, dp_zero1_update,
+ * dp_zero2_update) and the norm of the owner chunks (dp_grad_global_norm,
+ * dp_grad_global_norm_static).  That wait is bounded by the SM clock (about
+ * two seconds); if it runs out, the tile is left unprocessed and this flag is
+ * set, instead of the kernel hanging.  *flag_out = 1 if that happened since the last call, else 0.
  * Synchronous: call it after the work in question has finished (for example
  * after cudaStreamSynchronize), not inside a stream capture.  Returns
  * DPZ_ERR_INVALID_ARG for a NULL flag_out, DPZ_ERR_CUDA if the read fails. */

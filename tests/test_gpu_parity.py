@@ -88,6 +88,17 @@ def test_global_norm(N, C, gdt):
     dpz.dp_grad_global_norm(G, N, ws, nrm)
     gn = nrm.item()
     assert abs(gn - onorm) <= 1e-6 * onorm
+    # the staged norm kernel writes the same per-segment partials as the
+    # reduce kernel: the norm of the fused path is the same float
+    G2 = up(g)
+    nrm2 = torch.zeros(1, device=DEV)
+    ws2 = dpz.workspace(N * C, N, DEV)
+    T = torch.zeros(N * C, device=DEV)
+    W = torch.zeros(N * N * C, dtype=G2.dtype, device=DEV)
+    cfg = dpz.make_cfg(1e-3, 0.9, 0.999, 1e-8, 0.0, 1, 1e30)   # clip that never triggers
+    dpz.dp_zero1_step(G2, T, T.clone(), T.clone(), W, N, cfg, ws=ws2, norm_out=nrm2)
+    assert nrm2.item() == gn
+    assert dpz.device_status() == 0
 
 
 # ----------------------------------------------------------- the step
