@@ -157,3 +157,96 @@ def test_allreduce_sweep(N):
             assert same_bits(down(G).reshape(N, w.P), g), size
         else:
             _allreduce_full(w)
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+
+
+def _segment_buckets(P, N, k):
+    """k buckets on 256-element segment boundaries of their chunks, in
+    backward (last-first) order."""
+    C = P // N
+    edges = {0, P}
+    for i in range(1, k):
+        b = P * i // k
+        c = b // C
+        edges.add(c * C + (b - c * C) // 256 * 256)
+    edges = sorted(edges)
+    return [(edges[i], edges[i + 1] - edges[i]) for i in range(len(edges) - 1)][::-1]
+
+
+def test_buckets_and_zero2_full_size():
+    """The GPT-2 1.5B step in 16 buckets reduced on a side stream with the grid
+    capped at one block per SM (the bench's overlap configuration), then the
+    norm and dp_zero1_update; and as ZeRO-2 from a reused staging buffer into
+    gradient shards.  Both equal dp_zero1_step bit for bit: the same partials,
+    the same norm, the same averages, master/m/v and weights.  (dp_zero1_step
+    itself is checked against the oracle above.)"""
+    w = I.GPT2_1P5B
+    N, P, C = w.N, w.P, w.C
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip,
+                       store_avg=True)
+
+    def fresh():
+        G = torch.empty(N * P, dtype=torch.bfloat16, device=DEV)
+        I.fill_grads_device(w, G)
+        T = torch.empty(P, dtype=torch.float32, device=DEV)
+        M, V = torch.empty_like(T), torch.empty_like(T)
+        for which, t in (("master", T), ("m", M), ("v", V)):
+            I.fill_state_device(w, which, t)
+        return G, T, M, V, torch.zeros(N * P, dtype=torch.bfloat16, device=DEV)
+
+    G, T, M, V, W = fresh()
+    ws = dpz.workspace(P, N, DEV)
+    nrm = torch.zeros(1, device=DEV)
+    dpz.dp_zero1_step(G, T, M, V, W, N, cfg, ws=ws, norm_out=nrm)
+    owner = torch.cat([G.view(N, P)[c, c * C:(c + 1) * C] for c in range(N)])
+    del G
+    torch.cuda.empty_cache()
+
+    buckets = _segment_buckets(P, N, 16)
+    main = torch.cuda.current_stream()
+    comm = torch.cuda.Stream()
+
+    # ZeRO-1 in buckets, in place in the arena
+    Gb, Tb, Mb, Vb, Wb = fresh()
+    wsb = dpz.workspace(P, N, DEV)
+    nrmb = torch.zeros(1, device=DEV)
+    comm.wait_stream(main)
+    for lo, n in buckets:
+        dpz.dp_reduce_scatter_avg_range(Gb, N, lo, n, ws=wsb, stream=comm, max_ctas=sms)
+    dpz.dp_grad_norm_finalize(wsb, P, N, nrmb, stream=comm)
+    dpz.dp_zero1_update(Gb, Tb, Mb, Vb, Wb, N, cfg, ws=wsb, stream=comm)
+    main.wait_stream(comm)
+    torch.cuda.synchronize()
+    assert nrmb.item() == nrm.item()
+    owner_b = torch.cat([Gb.view(N, P)[c, c * C:(c + 1) * C] for c in range(N)])
+    assert torch.equal(_bits(owner_b), _bits(owner))
+    for got, want in ((Tb, T), (Mb, M), (Vb, V), (Wb, W)):
+        assert torch.equal(_bits(got), _bits(want))
+    del owner_b, Gb, Tb, Mb, Vb, Wb
+    torch.cuda.empty_cache()
+
+    # ZeRO-2: each bucket's N rows staged in one reused buffer, reduced into shards
+    src, T2, M2, V2, W2 = fresh()
+    src = src.view(N, P)
+    ws2 = dpz.workspace(P, N, DEV)
+    nrm2 = torch.zeros(1, device=DEV)
+    shards = torch.zeros(P, dtype=torch.bfloat16, device=DEV)
+    staging = torch.empty(N * max(n for _, n in buckets), dtype=torch.bfloat16, device=DEV)
+    for lo, n in buckets:
+        stage = staging[:N * n]
+        stage.view(N, n).copy_(src[:, lo:lo + n])
+        dpz.dp_reduce_scatter_avg_bucket(stage, lo, shards, N, ws=ws2, max_ctas=sms)
+    dpz.dp_grad_norm_finalize(ws2, P, N, nrm2)
+    dpz.dp_zero2_update(shards, T2, M2, V2, W2, N, cfg, ws=ws2)
+    torch.cuda.synchronize()
+    assert nrm2.item() == nrm.item()
+    assert torch.equal(_bits(shards), _bits(owner))
+    for got, want in ((T2, T), (M2, M), (V2, V), (W2, W)):
+        assert torch.equal(_bits(got), _bits(want))
+    assert dpz.device_status() == 0
+    del src, T2, M2, V2, W2, shards, staging, T, M, V, W, owner
+    torch.cuda.empty_cache()
