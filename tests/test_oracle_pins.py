@@ -66,6 +66,50 @@ def test_ring_every_rank_has_the_full_sum(N, rho):
         assert np.array_equal(a[r], want)
 
 
+@pytest.mark.parametrize("rho", [0, 1])
+@pytest.mark.parametrize("N", [4, 2, 3, 8])
+def test_ring_contribution_counts(N, rho):
+    """13.5 Multi-GPU from First Principles, 13.5.3 and Figure 13.5.3: with
+    every rank's input 1, a cell holds the number of the N contributions its
+    chunk has.  Each reduce-scatter step moves one chunk per link, so each rank
+    gains exactly one cell, which holds one more contribution than the
+    sender's copy: after step t a rank's counts are 2..t+2 and N-1-t ones.
+    After the phase every device owns one full chunk (N), a different chunk per
+    device.  Each all-gather step then completes one more cell per rank, until
+    all N x N cells are full."""
+    width = 3
+    ones = np.ones((N, N * width), dtype=np.float64)
+
+    def counts(a):
+        cells = a.reshape(N, N, width)
+        assert np.all(cells == cells[:, :, :1])          # a chunk moves as a whole
+        return cells[:, :, 0].astype(int)
+
+    prev = counts(ones)
+    for t in range(N - 1):
+        a = ones.copy()
+        sent = O.ring_reduce_scatter(a, rho=rho, steps=t + 1)
+        cur = counts(a)
+        assert np.all(sent == (t + 1) * width * 8)          # one chunk per link per step
+        for r in range(N):
+            assert sorted(cur[r]) == [1] * (N - 1 - t) + list(range(2, t + 3))
+            assert np.sum(cur[r] != prev[r]) == (1 if N > 1 else 0)
+        prev = cur
+    full = [int(np.flatnonzero(prev[r] == N)[0]) for r in range(N)]
+    assert all(np.sum(prev[r] == N) == 1 for r in range(N))
+    assert sorted(full) == list(range(N))                   # a different chunk per device
+    for r in range(N):
+        assert O.owner(full[r], N, rho=rho) == r
+    for t in range(N - 1):
+        a = ones.copy()
+        O.ring_reduce_scatter(a, rho=rho)
+        O.ring_allgather(a, rho=rho, steps=t + 1)
+        cur = counts(a)
+        for r in range(N):
+            assert np.sum(cur[r] == N) == t + 2
+    assert np.all(cur == N)
+
+
 def test_owner_with_rotation_one_is_zero1_shard_offset():
     """A4 Part 2: rank r's shard starts at r * shard_size, so with rho = 1
     rank c owns chunk c."""
