@@ -1,8 +1,10 @@
 // Optimizer-side kernel: sharded AdamW on every rank's owned chunk, the cast
 // to the weight dtype, and the write of the new weights into the owner slab
-// (zero1_adamw_step) or into all N slabs (the fused all-gather).  The averaged
-// gradient is either loaded from the owner slab (after a reduce-scatter) or
-// computed in place by the ring fold (the single-kernel step without clip).
+// (zero1_adamw_step, averages loaded from the owner slab) or into all N slabs
+// (the single-kernel step without clip, averages computed in place by the
+// ring fold).  AdamW + all-gather from stored averages (the clipped step,
+// dp_zero1_update, dp_zero2_update) is the bulk-copy staged kernel of
+// staged.cu, to which launch_adamw hands that case.
 #include "device.cuh"
 #include "internal.h"
 
@@ -15,8 +17,8 @@ namespace dpz {
 // the arena, 0 for a compact [P] buffer of gradient shards.
 // One-shot grid, one segment per warp (device.cuh).  Register caps that keep
 // more blocks, hence more loads, in flight: 64 registers (four blocks per SM)
-// wherever that does not spill, which is every load-owner variant and the
-// fold over up to four bf16 slabs; 80 (three blocks) for the other folds.
+// wherever that does not spill, which is the load-owner variant and the fold
+// over up to four bf16 slabs; 80 (three blocks) for the other folds.
 template <int GDT, int NT, bool FOLD>
 struct AdamwBlocksPerSm {
     static constexpr int value = !FOLD || (GDT != 0 && NT > 0 && NT <= 4) ? 4 : 3;
