@@ -412,13 +412,15 @@ def run_gpu(args) -> None:
     cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)
     stream = torch.cuda.current_stream()
 
-    def full_step(on=None):
-        on = stream if on is None else on
+    def step_with(grads, on):
         if w.allreduce_only:
-            dpz.dp_allreduce_avg(G, w.N, on, acc32=args.acc32)
+            dpz.dp_allreduce_avg(grads, w.N, on, acc32=args.acc32)
         else:
-            dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=on,
+            dpz.dp_zero1_step(grads, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=on,
                               acc32=args.acc32)
+
+    def full_step(on=None):
+        step_with(G, stream if on is None else on)
 
     step = full_step
     if args.entry != "step":
@@ -487,7 +489,7 @@ def run_gpu(args) -> None:
     e2e = None
     if not args.no_e2e:
         full = None if w.allreduce_only or w.clip <= 0 else (T, M, V, W, ws, cfg)
-        e2e = run_e2e(args, w, G, step, nrm, stream, world, full)
+        e2e = run_e2e(args, w, G, step_with, nrm, stream, world, full)
 
     cpu = cpu_mt = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -638,13 +640,22 @@ def run_graph(args, step, stream, world, nbytes):
             "value": round(nbytes * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT}
 
 
-def run_e2e(args, w, G, step, nrm, stream, world, full=None):
+def run_e2e(args, w, G, step_with, nrm, stream, world, full=None):
     """The step through the public API with the gradients coming from pinned
-    host memory and the norm read back, every step.  Pipelined: the host-to-
-    device copy of bucket b (a copy engine, one stream) overlaps the reduce-
-    scatter of bucket b-1 (dp_reduce_scatter_avg_range on a second stream,
-    ordered by an event per bucket); then the norm and the update.  The plain
-    form (copy everything, then dp_zero1_step) is timed too."""
+    host memory and the step's result (the norm; for an all-reduce one
+    element) read back, every step.
+
+    - Prefetched (the reported value unless --e2e-buckets is given): two
+      gradient arenas; the host-to-device copy of step k+1's gradients runs on
+      a copy stream while step k computes on the other arena, as a training
+      loop prefetches its next batch.  Every step still copies its whole input
+      and reads its result back; K steps are timed from the first copy to the
+      last read, prologue and epilogue included.
+    - Plain (always timed, reported as plain_ms_per_step): copy, then step.
+    - --e2e-buckets K: within one step, the copy of bucket b (a copy engine,
+      one stream) overlaps the reduce-scatter of bucket b-1
+      (dp_reduce_scatter_avg_range on a second stream, ordered by an event
+      per bucket); then the norm and the update."""
     import torch
     import gradient_reduction_zero_gb300.dpz as dpz
     host = torch.empty(G.shape, dtype=G.dtype, pin_memory=True)
@@ -652,10 +663,13 @@ def run_e2e(args, w, G, step, nrm, stream, world, full=None):
     torch.cuda.synchronize()
     Gv, Hv = G.view(w.N, w.P), host.view(w.N, w.P)
 
+    def result(buf):
+        return nrm.item() if not w.allreduce_only else buf[:1].item()
+
     def plain():
         G.copy_(host, non_blocking=True)
-        step()
-        return nrm.item() if not w.allreduce_only else G[:1].item()
+        step_with(G, stream)
+        return result(G)
 
     copy_s = torch.cuda.Stream()
     comm = torch.cuda.Stream(priority=-1)
@@ -689,19 +703,59 @@ def run_e2e(args, w, G, step, nrm, stream, world, full=None):
         torch.cuda.synchronize()
         return max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, world)
 
+    def prefetched_run(k):
+        """k steps, double-buffered; returns seconds per step."""
+        bufs = (G, G2)
+        freed = [None, None]          # event: the last step that used the arena is done
+
+        def copy_in(i):
+            b = i % 2
+            if freed[b] is not None:
+                copy_s.wait_event(freed[b])
+            with torch.cuda.stream(copy_s):
+                bufs[b].copy_(host, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(copy_s)
+            return ev
+
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        ready = copy_in(0)
+        for i in range(k):
+            nxt = copy_in(i + 1) if i + 1 < k else None     # overlaps step i
+            stream.wait_event(ready)
+            step_with(bufs[i % 2], stream)
+            done = torch.cuda.Event()
+            done.record(stream)
+            freed[i % 2] = done
+            result(bufs[i % 2])                              # the read-back, every step
+            ready = nxt
+        torch.cuda.synchronize()
+        return max_over_ranks((time.perf_counter() - t0) / k, world)
+
     dt_plain = timed(plain)
     use_pipe = full is not None and args.e2e_buckets > 1
-    dt = timed(pipelined) if use_pipe else dt_plain
+    if use_pipe:
+        dt = timed(pipelined)
+        how = (f"pinned host gradients, {len(buckets)} buckets copied on one stream and "
+               "reduced on another (dp_reduce_scatter_avg_range, events), then "
+               "dp_grad_norm_finalize + dp_zero1_update; norm read back")
+    else:
+        G2 = torch.empty_like(G)
+        prefetched_run(2)                                    # warm-up
+        dt = prefetched_run(max(3, args.e2e_steps))
+        del G2
+        call = "dp_allreduce_avg" if w.allreduce_only else "dp_zero1_step"
+        what = "one element" if w.allreduce_only else "the norm"
+        how = (f"pinned host gradients copied on a copy stream into one of two arenas while "
+               f"the previous step runs ({call}), {what} read back every step; "
+               f"{max(3, args.e2e_steps)} steps timed from the first copy to the last read")
     d2h = 4 if not w.allreduce_only else G.element_size()
     out = {"value": round(step_bytes(w) * world / dt / 1e9, 2), "unit": UNIT,
            "ms_per_step": round(dt * 1e3, 3),
            "h2d_bytes_per_step": G.numel() * G.element_size(), "d2h_bytes_per_step": d2h,
-           "how": (f"pinned host gradients, {len(buckets)} buckets copied on one stream and "
-                   "reduced on another (dp_reduce_scatter_avg_range, events), then "
-                   "dp_grad_norm_finalize + dp_zero1_update; norm read back")
-           if use_pipe else ("pinned host gradients copied, dp_allreduce_avg, one element read "
-                             "back" if w.allreduce_only else
-                             "pinned host gradients copied, dp_zero1_step, norm read back"),
+           "how": how,
            "plain_ms_per_step": round(dt_plain * 1e3, 3)}
     return out
 
@@ -713,7 +767,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["dpz", "reference"], default="dpz")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-buckets", type=int, default=0,
                     help="> 1: pipeline the e2e host copies with bucketed reduce-scatters")
     ap.add_argument("--entry", choices=ENTRIES, default="step",
