@@ -24,6 +24,69 @@ struct AdamwBlocksPerSm {
     static constexpr int value = !FOLD || (GDT != 0 && NT > 0 && NT <= 4) ? 4 : 3;
 };
 
+// The work of one lane: group gi of chunk c (nothing if gi is past the chunk
+// end).  Returns the lane's sum of squares of its averaged values (SUMSQ),
+// else 0.
+template <int GDT, int WDT, int NT, bool FOLD, bool BCAST, bool SUMSQ>
+__device__ __forceinline__ float adamw_group(char* __restrict__ grads, float* __restrict__ master,
+                                             float* __restrict__ mom, float* __restrict__ var,
+                                             char* __restrict__ weights, int64_t P, int64_t C,
+                                             int N, int c, int64_t gi, const Avg& avg,
+                                             const AdamArgs& h, int store_avg, bool do_scale,
+                                             float scale, int64_t avg_stride)
+{
+    constexpr int GES = Group<GDT>::kBytes;
+    constexpr int WES = Group<WDT>::kBytes;
+    const int64_t gslab = P * GES;
+    const int64_t wslab = P * WES;
+    float ss = 0.0f;
+    if (gi >= C / kGroup) return ss;
+    const int64_t e = c * C + gi * kGroup;      // element index (same in every slab)
+    constexpr int NS = NT > 0 ? NT : 1;
+    const char* src[NS];
+    if constexpr (NT > 0) ring_sources<NT>(grads, gslab, c, src);
+    float g[8];
+    if (FOLD) {
+        if constexpr (NT > 0) {
+            typename Group<GDT>::Raw raw[NT];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) raw[j] = Group<GDT>::load_raw(src[j] + e * GES);
+            fold_loaded<GDT, NT>(raw, g);
+        } else {
+            ring_fold<GDT>(grads, gslab, e * GES, c, N, g);
+        }
+        average8<GDT>(g, avg);
+        if (SUMSQ) ss = sumsq8(g);
+        if (store_avg) store_group<GDT>(grads + c * gslab + e * GES, g);
+    } else {
+        load_group<GDT>(grads + (c * avg_stride + e) * GES, g);
+    }
+    float th[8], mm[8], vv[8];
+    load_group<0>(reinterpret_cast<const char*>(master + e), th);
+    load_group<0>(reinterpret_cast<const char*>(mom + e), mm);
+    load_group<0>(reinterpret_cast<const char*>(var + e), vv);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float gq = do_scale ? __fmul_rn(g[q], scale) : g[q];
+        adamw_elem(th[q], mm[q], vv[q], gq, h);
+    }
+    store_group<0>(reinterpret_cast<char*>(master + e), th);
+    store_group<0>(reinterpret_cast<char*>(mom + e), mm);
+    store_group<0>(reinterpret_cast<char*>(var + e), vv);
+    const typename Group<WDT>::Raw w = Group<WDT>::pack(th);
+    if (BCAST) {
+        if constexpr (NT > 0) {
+#pragma unroll
+            for (int r = 0; r < NT; ++r) Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
+        } else {
+            for (int r = 0; r < N; ++r) Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
+        }
+    } else {
+        Group<WDT>::store_raw(weights + c * wslab + e * WES, w);
+    }
+    return ss;
+}
+
 template <int GDT, int WDT, int NT, bool FOLD, bool BCAST, bool SUMSQ>
 __global__ void __launch_bounds__(kBlock, AdamwBlocksPerSm<GDT, NT, FOLD>::value)
 k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
@@ -32,19 +95,12 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
         double* __restrict__ partials, int64_t avg_stride)
 {
     const int N = NT > 0 ? NT : n_rt;
-    constexpr int GES = Group<GDT>::kBytes;
-    constexpr int WES = Group<WDT>::kBytes;
-    const int64_t gslab = P * GES;
-    const int64_t wslab = P * WES;
-    const int64_t groups = C / kGroup;
     const int64_t segs = segments_per_chunk(C);
     const int lane = threadIdx.x & 31;
     if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     const int64_t sw = global_warp();
     if (sw >= (int64_t)N * segs) return;                 // whole warps
     const SegPos p = seg_pos(sw, segs);
-    const int c = p.c;
-    const int64_t gi = p.seg * 32 + lane;
 
     // clip scale from the global norm of the averaged gradient
     float scale = 1.0f;
@@ -57,57 +113,52 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
         }
     }
 
-    float ss = 0.0f;
-    if (gi < groups) {
-        const int64_t e = c * C + gi * kGroup;  // element index (same in every slab)
-        constexpr int NS = NT > 0 ? NT : 1;
-        const char* src[NS];
-        if constexpr (NT > 0) ring_sources<NT>(grads, gslab, c, src);
-        float g[8];
-        if (FOLD) {
-            if constexpr (NT > 0) {
-                typename Group<GDT>::Raw raw[NT];
-#pragma unroll
-                for (int j = 0; j < NT; ++j) raw[j] = Group<GDT>::load_raw(src[j] + e * GES);
-                fold_loaded<GDT, NT>(raw, g);
-            } else {
-                ring_fold<GDT>(grads, gslab, e * GES, c, N, g);
-            }
-            average8<GDT>(g, avg);
-            if (SUMSQ) ss = sumsq8(g);
-            if (store_avg) store_group<GDT>(grads + c * gslab + e * GES, g);
-        } else {
-            load_group<GDT>(grads + (c * avg_stride + e) * GES, g);
-        }
-        float th[8], mm[8], vv[8];
-        load_group<0>(reinterpret_cast<const char*>(master + e), th);
-        load_group<0>(reinterpret_cast<const char*>(mom + e), mm);
-        load_group<0>(reinterpret_cast<const char*>(var + e), vv);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float gq = do_scale ? __fmul_rn(g[q], scale) : g[q];
-            adamw_elem(th[q], mm[q], vv[q], gq, h);
-        }
-        store_group<0>(reinterpret_cast<char*>(master + e), th);
-        store_group<0>(reinterpret_cast<char*>(mom + e), mm);
-        store_group<0>(reinterpret_cast<char*>(var + e), vv);
-        const typename Group<WDT>::Raw w = Group<WDT>::pack(th);
-        if (BCAST) {
-            if constexpr (NT > 0) {
-#pragma unroll
-                for (int r = 0; r < NT; ++r)
-                    Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
-            } else {
-                for (int r = 0; r < N; ++r)
-                    Group<WDT>::store_raw(weights + r * wslab + e * WES, w);
-            }
-        } else {
-            Group<WDT>::store_raw(weights + c * wslab + e * WES, w);
-        }
-    }
+    const float ss = adamw_group<GDT, WDT, NT, FOLD, BCAST, SUMSQ>(
+        grads, master, mom, var, weights, P, C, N, p.c, p.seg * 32 + lane, avg, h, store_avg,
+        do_scale, scale, avg_stride);
     if (SUMSQ) {
         const float t = warp_sum_f32(ss);
-        if (lane == 0) partials[c * segs + p.seg] = (double)t;
+        if (lane == 0) partials[p.c * segs + p.seg] = (double)t;
+    }
+}
+
+// The whole step without clip for a small arena, norm included, in one block
+// of kFinalThreads (512) threads: each of the 16 warps takes segments w,
+// w + 16, ... of the list; then the block adds the segment partials exactly
+// as k_norm_finalize does when it runs as one block (lane t adds partials t,
+// t + 512, ... in order, then block_sum), and its second level only adds that
+// value to zeros.  So the norm has the same bits as the two-kernel path, in
+// one launch instead of two for arenas of at most kSmallStepSegments
+// segments, where launch latency is the cost.
+template <int GDT, int WDT>
+__global__ void __launch_bounds__(kFinalThreads)
+k_zero1_small(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
+              float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int N,
+              Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
+              double* __restrict__ partials, float* __restrict__ norm_out)
+{
+    const int64_t segs = segments_per_chunk(C);
+    const int64_t total = (int64_t)N * segs;
+    const int lane = threadIdx.x & 31;
+    for (int64_t sw = threadIdx.x >> 5; sw < total; sw += kFinalThreads / 32) {  // whole warps
+        const SegPos p = seg_pos(sw, segs);
+        const float ss = adamw_group<GDT, WDT, 0, true, true, true>(
+            grads, master, mom, var, weights, P, C, N, p.c, p.seg * 32 + lane, avg, h,
+            store_avg, false, 1.0f, P);
+        const float t = warp_sum_f32(ss);
+        if (lane == 0) partials[p.c * segs + p.seg] = (double)t;
+    }
+    __syncthreads();     // every partial of the block is written and visible
+    double v = 0.0;
+    for (int64_t i = threadIdx.x; i < total; i += kFinalThreads) v += partials[i];
+    const double r = block_sum(v);
+    if (threadIdx.x == 0) {
+        const float nrm = __double2float_rn(__dsqrt_rn(r));
+        hdr->sumsq = r;
+        hdr->norm = nrm;
+        hdr->nparts = (uint32_t)total;
+        hdr->arrive = 0u;
+        if (norm_out) *norm_out = nrm;
     }
 }
 
@@ -167,6 +218,35 @@ static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, A
         return launch_adamw_bcast_tma(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     return adamw_t<GDT, WDT, 0, false, false, false>(a, avg, h, false, grads, master, m, v,
                                                     weights, ws, s, avg_stride);
+}
+
+bool zero1_fits_one_block(const Arena& a)
+{
+    return int64_t(a.N) * segments_per_chunk(a.C) <= kSmallStepSegments;
+}
+
+cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
+                               void* grads, float* master, float* m, float* v, void* weights,
+                               void* ws, float* norm_out, cudaStream_t s)
+{
+    set_last_kernel_name("dpz_zero1_small");
+    char* g = static_cast<char*>(grads);
+    char* w = static_cast<char*>(weights);
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    double* parts = ws_partials(ws);
+    const int sa = store_avg ? 1 : 0;
+#define DPZ_SMALL(GD, WD)                                                                      \
+    k_zero1_small<GD, WD><<<1, kFinalThreads, 0, s>>>(g, master, m, v, w, a.P, a.C, a.N, avg, \
+                                                      h, sa, hdr, parts, norm_out)
+    if (a.gdt == 2) {
+        if (a.wdt == 1) DPZ_SMALL(2, 1); else DPZ_SMALL(2, 0);
+    } else if (a.gdt == 1) {
+        if (a.wdt == 1) DPZ_SMALL(1, 1); else DPZ_SMALL(1, 0);
+    } else {
+        if (a.wdt == 1) DPZ_SMALL(0, 1); else DPZ_SMALL(0, 0);
+    }
+#undef DPZ_SMALL
+    return cudaGetLastError();
 }
 
 cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,

@@ -102,6 +102,15 @@ cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, Adam
                          int64_t avg_stride);
 cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 
+// The whole step without clip, norm included, in one single-block launch, for
+// arenas of at most kSmallStepSegments 256-element segments (adamw.cu).  Same
+// results, bit for bit, as the fold kernel plus launch_norm_finalize.
+constexpr int64_t kSmallStepSegments = 32;
+bool zero1_fits_one_block(const Arena& a);
+cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
+                               void* grads, float* master, float* m, float* v, void* weights,
+                               void* ws, float* norm_out, cudaStream_t s);
+
 // AdamW + cast + all-gather from the stored averages (element e of chunk c
 // at grads + c*avg_stride + e), staged through shared memory by bulk copies
 // (staged.cu, as is launch_norm_owned).  A tile that does not arrive within

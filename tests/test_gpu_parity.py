@@ -188,6 +188,25 @@ def test_fused_equals_unfused(N, C, clip):
     assert a[5] == b[5]
 
 
+@pytest.mark.parametrize("N,C,launches", [(4, 2048, 1), (3, 2816, 2), (4, 1024, 1), (1, 8, 1),
+                                           (8, 1024, 1), (8, 1032, 2)])
+@pytest.mark.parametrize("gdt", ["f32", "bf16"])
+def test_small_step_is_one_launch_and_identical(N, C, launches, gdt):
+    """Without clip and with the norm wanted, an arena of at most 32 segments
+    runs the step and its norm in one single-block launch; larger ones use the
+    fold kernel plus the finalisation.  Both give the four separate calls'
+    bits, the norm included."""
+    w, g, th, m, v, wts = make_problem(N, C, gdt, "bf16", 0.0, seed=C + N)
+    before = dpz.launch_count()
+    a = run_gpu_step(w, g, th, m, v, wts, fused=True)
+    assert dpz.launch_count() - before == launches
+    b = run_gpu_step(w, g, th, m, v, wts, fused=False)
+    for x, y in zip(a[:5], b[:5]):
+        assert same_bits(x, y)
+    assert a[5] == b[5]
+    check_step(w, g, th, m, v, wts, a)
+
+
 @pytest.mark.parametrize("store_avg,want_norm", [(False, False), (False, True), (True, False)])
 def test_no_clip_variants(store_avg, want_norm):
     N, C = 4, 6152
