@@ -238,6 +238,7 @@ def time_oracle(w: I.Workload, seconds: float) -> dict:
         done_bytes += step_bytes(mini)
         reps += 1
     return {"value": done_bytes / elapsed / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "steps_per_s": done_bytes / elapsed / step_bytes(w),
             "sample": f"{reps} windows of {width} elements per chunk x {w.N} chunks x {w.N} ranks "
                       f"of {w.name} ({elapsed:.1f} s single-threaded)"}
 
@@ -280,7 +281,7 @@ def time_oracle_threads(w: I.Workload, seconds: float, threads: int) -> dict:
     elapsed = time.perf_counter() - t0
     done = sum(counts)
     return {"value": done * step_bytes(mini) / elapsed / 1e9, "unit": UNIT, "cores": threads,
-            "kind": "oracle",
+            "kind": "oracle", "steps_per_s": done * step_bytes(mini) / elapsed / step_bytes(w),
             "sample": f"{done} windows of {width} elements per chunk x {w.N} chunks x {w.N} ranks "
                       f"of {w.name} on {threads} host threads, disjoint windows "
                       f"({elapsed:.1f} s wall)"}
@@ -303,6 +304,7 @@ def run_reference(args) -> None:
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_bytes(w) / (value * 1e9) * 1e3,
+            "steps_per_s": value * 1e9 / step_bytes(w),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": config_of(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
