@@ -250,3 +250,49 @@ def test_buckets_and_zero2_full_size():
     assert dpz.device_status() == 0
     del src, T2, M2, V2, W2, shards, staging, T, M, V, W, owner
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("clip", [1.0, 0.0], ids=["clip", "no-clip"])
+def test_graph_replay_full_size(clip):
+    """The GPT-2 1.5B step captured in a CUDA graph (as bench --graph times it)
+    and replayed twice equals two eager steps on a fresh copy of the inputs,
+    bit for bit: the calls only enqueue kernels, and every run of the step is
+    deterministic."""
+    w = I.GPT2_1P5B.with_(clip=clip)
+    N, P = w.N, w.P
+    cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)
+
+    def fresh():
+        G = torch.empty(N * P, dtype=torch.bfloat16, device=DEV)
+        I.fill_grads_device(w, G)
+        T = torch.empty(P, dtype=torch.float32, device=DEV)
+        M, V = torch.empty_like(T), torch.empty_like(T)
+        for which, t in (("master", T), ("m", M), ("v", V)):
+            I.fill_state_device(w, which, t)
+        return [G, T, M, V, torch.zeros(N * P, dtype=torch.bfloat16, device=DEV)]
+
+    eager = fresh()
+    ws_e, n_e = dpz.workspace(P, N, DEV), torch.zeros(1, device=DEV)
+    for _ in range(2):
+        dpz.dp_zero1_step(*eager, N, cfg, ws=ws_e, norm_out=n_e)
+    torch.cuda.synchronize()
+    eager_bits = [_bits(t).clone() for t in eager[1:]]     # master, m, v, weights
+    del eager
+    torch.cuda.empty_cache()
+
+    graph = fresh()
+    ws_g, n_g = dpz.workspace(P, N, DEV), torch.zeros(1, device=DEV)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        dpz.dp_zero1_step(*graph, N, cfg, ws=ws_g, norm_out=n_g)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert n_g.item() == n_e.item()
+    for got, want in zip(graph[1:], eager_bits):
+        assert torch.equal(_bits(got), want)
+    assert dpz.device_status() == 0
+    del graph, eager_bits, g
+    torch.cuda.empty_cache()
