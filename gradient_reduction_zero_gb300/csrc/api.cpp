@@ -203,6 +203,14 @@ DPZ_API const char* dpz_version(void) { return "dpz 0.1 (sm_103a)"; }
 
 DPZ_API int64_t dpz_launch_count(void) { return g_launches.load(); }
 
+DPZ_API int dpz_selftest_staged_timeout(void* buf, void* stream)
+{
+    DPZ_TRY(check_ptr(buf, "buf"));
+    cudaStream_t s = as_stream(stream);
+    DPZ_TRY(launch(s, [&] { return launch_staged_timeout_selftest(buf, s); }));
+    return ok();
+}
+
 DPZ_API int dpz_device_status(int* flag_out)
 {
     if (flag_out == nullptr) return fail(DPZ_ERR_INVALID_ARG, "flag_out is NULL");

@@ -120,6 +120,9 @@ cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void
                                    int64_t avg_stride, float* master, float* m, float* v,
                                    void* weights, const void* ws, cudaStream_t s);
 cudaError_t read_and_clear_pipeline_error(unsigned* flag);
+// Launch the staged AdamW kernel on a one-tile arena in `buf` (256 bytes)
+// with a barrier that never completes, so that its bounded wait runs out.
+cudaError_t launch_staged_timeout_selftest(void* buf, cudaStream_t s);
 
 
 // The fixed device scratch of dp_grad_global_norm_static (norm_static.cu):

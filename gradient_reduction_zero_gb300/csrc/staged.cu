@@ -53,11 +53,15 @@ struct TmaTile {
 // grads: the averaged gradient of element e (chunk c) at grads + (c*avg_stride
 // + e) elements; hdr: the workspace header (the norm), read when clip > 0.
 // NT > 0: N == NT known at compile time; NT == 0: any N, read from n_rt.
+// extra_tx: bytes the barrier expects beyond the tile's loads, 0 except in
+// the self-test of the timeout path (dpz_selftest_staged_timeout), where the
+// barrier then never completes and the bounded wait runs out.
 template <int GDT, int WDT, int NT>
 __global__ void __launch_bounds__(kTmaThreads)
 k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __restrict__ master,
                   float* __restrict__ mom, float* __restrict__ var, char* __restrict__ weights,
-                  int64_t P, int64_t C, int n_rt, AdamArgs h, const WsHeader* __restrict__ hdr)
+                  int64_t P, int64_t C, int n_rt, AdamArgs h, const WsHeader* __restrict__ hdr,
+                  uint32_t extra_tx)
 {
     using GS = Group<GDT>;
     using WS = Group<WDT>;
@@ -81,7 +85,7 @@ k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __r
     if (tid == 0) {
         mbar_init_one(&full);
         timed_out = 0;
-        mbar_expect_tx(&full, (uint32_t)n * (GES + 12u));
+        mbar_expect_tx(&full, (uint32_t)n * (GES + 12u) + extra_tx);
         bulk_load(t.avg, grads + ((int64_t)c * avg_stride + e) * GES, (uint32_t)n * GES, &full);
         bulk_load(t.th, master + e, (uint32_t)n * 4u, &full);
         bulk_load(t.m, mom + e, (uint32_t)n * 4u, &full);
@@ -234,8 +238,8 @@ cudaError_t tma_t(const Arena& a, const AdamArgs& h, const void* grads, int64_t 
     set_last_kernel_name("dpz_adamw_bcast");
     fn<<<(unsigned)tiles, kTmaThreads, smem, s>>>(static_cast<const char*>(grads), avg_stride,
                                                   master, m, v, static_cast<char*>(weights), a.P,
-                                                  a.C, a.N, h,
-                                                  static_cast<const WsHeader*>(ws));
+                                                  a.C, a.N, h, static_cast<const WsHeader*>(ws),
+                                                  0u);
     return cudaGetLastError();
 }
 
@@ -284,6 +288,37 @@ cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaS
     set_last_kernel_name("dpz_norm_owned");
     // both bf16 modes store bf16 averages
     return a.gdt != 0 ? norm_t<1>(a, grads, ws, s) : norm_t<0>(a, grads, ws, s);
+}
+
+// The self-test of the timeout path: the staged AdamW kernel on a one-tile
+// arena (N = 1, P = 8, bf16 averages and weights, fp32 state) laid out in the
+// caller's buffer, with a barrier that expects 16 bytes more than the four
+// loads deliver.  Every copy it issues completes, so nothing is in flight
+// when the CTA gives up; the bounded wait runs out (about two seconds, then
+// the bounded wait of the abandon path), the device flag is set, and the
+// kernel returns without writing.
+cudaError_t launch_staged_timeout_selftest(void* buf, cudaStream_t s)
+{
+    auto fn = k_adamw_bcast_tma<1, 1, 1>;
+    const size_t smem = sizeof(TmaTile<1, 1>);
+    const cudaError_t e = allow_smem(reinterpret_cast<const void*>(fn), smem);
+    if (e != cudaSuccess) return e;
+    char* b = static_cast<char*>(buf);
+    AdamArgs h{};
+    h.lr = 1e-3f;
+    h.b1 = 0.9f;
+    h.b2 = 0.999f;
+    h.omb1 = 0.1f;
+    h.omb2 = 0.001f;
+    h.bc1 = 0.1f;
+    h.bc2 = 0.001f;
+    h.eps = 1e-8f;
+    set_last_kernel_name("dpz_selftest_staged_timeout");
+    fn<<<1, kTmaThreads, smem, s>>>(b, 8, reinterpret_cast<float*>(b + 32),
+                                   reinterpret_cast<float*>(b + 64),
+                                   reinterpret_cast<float*>(b + 96), b + 128, 8, 8, 1, h,
+                                   nullptr, 16u);
+    return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_pipeline_error(unsigned* flag)

@@ -69,6 +69,7 @@ _SIGS = {
     "dpz_version": ([], ctypes.c_char_p),
     "dpz_launch_count": ([], ctypes.c_int64),
     "dpz_device_status": ([ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+    "dpz_selftest_staged_timeout": ([_VP, _VP], ctypes.c_int),
     "dpz_profile_start": ([ctypes.c_int], ctypes.c_int),
     "dpz_profile_stop": ([ctypes.POINTER(KernelStat), ctypes.c_int,
                           ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
@@ -241,6 +242,19 @@ def device_status() -> int:
     f = ctypes.c_int()
     _check(lib.dpz_device_status(ctypes.byref(f)))
     return f.value
+
+
+SELFTEST_BUF_BYTES = 256
+
+
+def selftest_staged_timeout(buf, stream=None) -> None:
+    """Launch the staged AdamW kernel on a one-tile arena in `buf` (a device
+    tensor of at least SELFTEST_BUF_BYTES bytes) with a barrier that never
+    completes, so that its bounded wait runs out and sets the device flag
+    (about four seconds)."""
+    if buf.numel() * buf.element_size() < SELFTEST_BUF_BYTES:
+        raise ValueError(f"buf must hold at least {SELFTEST_BUF_BYTES} bytes")
+    _check(lib.dpz_selftest_staged_timeout(_ptr(buf), _stream_handle(stream)))
 
 
 def version() -> str:

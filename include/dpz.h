@@ -295,6 +295,20 @@ DPZ_API const char* dpz_version(void);
  * DPZ_ERR_INVALID_ARG for a NULL flag_out, DPZ_ERR_CUDA if the read fails. */
 DPZ_API int dpz_device_status(int* flag_out);
 
+/* Self-test of the timeout path behind dpz_device_status (no counterpart on
+ * the pages).  Launches, on `stream`, the staged AdamW + all-gather kernel on
+ * a one-tile arena laid out in `buf`: DPZ_SELFTEST_BUF_BYTES bytes of caller
+ * device memory, 16-byte aligned (bf16 averages at +0, fp32 master/m/v at
+ * +32/+64/+96, bf16 weights at +128, 8 elements each).  Its barrier expects
+ * 16 bytes more than its bulk loads deliver; every copy it issues completes,
+ * so the wait runs out, after about two seconds plus the abandon path's
+ * bounded wait.  The kernel then sets the device flag and returns without
+ * writing `buf`.  After synchronising, dpz_device_status reports 1 and the
+ * context is usable.  Returns DPZ_ERR_INVALID_ARG for a NULL or misaligned
+ * buf, DPZ_ERR_CUDA if the launch fails. */
+#define DPZ_SELFTEST_BUF_BYTES 256
+DPZ_API int dpz_selftest_staged_timeout(void* buf, void* stream);
+
 /* Number of kernels this library has launched since it was loaded. */
 DPZ_API int64_t dpz_launch_count(void);
 

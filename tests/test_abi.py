@@ -165,3 +165,8 @@ def test_bucket_calls_reject(dpz):
 def test_device_status_rejects_null(dpz):
     assert dpz.lib.dpz_device_status(None) == 1
     assert b"flag_out" in dpz.lib.dpz_last_error()
+
+
+def test_selftest_rejects_bad_buffer(dpz):
+    assert dpz.lib.dpz_selftest_staged_timeout(None, None) == 1
+    assert dpz.lib.dpz_selftest_staged_timeout(A + 8, None) == 2        # misaligned
