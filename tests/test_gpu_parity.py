@@ -237,6 +237,25 @@ def test_staged_update_equals_owner_update_plus_allgather(gdt, wdt, N, C):
     check_step(w, g, th, m, v, wts, a)
 
 
+@pytest.mark.parametrize("N,C", [(4, 6152), (3, 1000)])
+def test_clip_boundary(N, C):
+    """The clip scales only when norm > clip: with clip equal to the norm the
+    clipped (three-kernel) step gives the unclipped step's bits; one float
+    below the norm it scales, as the oracle does with the same clip."""
+    w, g, th, m, v, wts = make_problem(N, C, "bf16", "bf16", 0.0, seed=31)
+    base = run_gpu_step(w, g, th, m, v, wts)                  # no clip; its norm
+    norm = np.float32(base[5])
+    at = w.with_(clip=float(norm))
+    out = run_gpu_step(at, g, th, m, v, wts)
+    assert out[5] == base[5]
+    for x, y in zip(out[1:5], base[1:5]):                    # master, m, v, weights
+        assert same_bits(x, y)
+    below = w.with_(clip=float(np.nextafter(norm, np.float32(0))))
+    out2 = run_gpu_step(below, g, th, m, v, wts)
+    assert not same_bits(out2[1], base[1])                   # scaled this time
+    check_step(below, g, th, m, v, wts, out2)
+
+
 def test_deterministic():
     w, g, th, m, v, wts = make_problem(8, 12344, "bf16", "bf16", 1e-3, seed=1)
     a = run_gpu_step(w, g, th, m, v, wts)
