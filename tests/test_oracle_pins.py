@@ -287,6 +287,51 @@ def test_averaging_identity_least_squares():
     np.testing.assert_allclose(summed[0, :d], N * full, rtol=1e-12)
 
 
+def test_one_step_one_device_vs_two_shards():
+    """13.5 Multi-GPU from First Principles, 13.5.2: one step on one device
+    with the whole batch and one step on k = 2 devices with half a batch each
+    (mean-loss gradients, averaged) differ only by rounding (the pages measure
+    about 1e-9).  Here: the ZeRO-1 step at N = 2 on the shards' gradients
+    against N = 1 on the full-batch gradient, least squares, AdamW mid-run
+    (m, v nonzero, t = 1000) so that the update depends on the gradient's
+    size: a sum instead of an average would move it by far more."""
+    rng = np.random.default_rng(7)
+    n, d, P = 256, 5, 16                              # P: 5 parameters, zero padded
+    X = rng.standard_normal((n, d))
+    y = rng.standard_normal(n)
+    w0 = np.zeros(P, dtype=np.float32)
+    w0[:d] = rng.standard_normal(d) * 0.02
+    m0 = np.zeros(P, dtype=np.float32)
+    v0 = np.zeros(P, dtype=np.float32)
+    m0[:d] = rng.standard_normal(d) * 1e-2
+    v0[:d] = np.abs(rng.standard_normal(d)) * 1e-3
+    w = w0[:d].astype(np.float64)
+
+    def grad(rows):
+        g = np.zeros(P, dtype=np.float32)
+        Xk, yk = X[rows], y[rows]
+        g[:d] = (Xk.T @ (Xk @ w - yk) / len(yk)).astype(np.float32)
+        return g
+
+    cfg = O.cfg_of(1e-3, 0.9, 0.999, 1e-8, 0.1, 1000)
+
+    def step(arena):
+        N = arena.shape[0]
+        th, m, v = w0.copy(), m0.copy(), v0.copy()
+        O.zero1_step(arena, th, m, v, np.zeros((N, P), dtype=np.uint16), cfg)
+        return th
+
+    one = step(grad(slice(0, n))[None, :].copy())
+    two = step(np.stack([grad(slice(0, n // 2)), grad(slice(n // 2, n))]))
+    delta = np.abs(one.astype(np.float64) - two.astype(np.float64))
+    assert delta.max() <= 1e-8, delta.max()
+    assert np.all(two[d:] == 0.0) and np.all(one[d:] == 0.0)
+    # the common bug: the sum of the shard gradients instead of their mean
+    summed = np.stack([grad(slice(0, n // 2)), grad(slice(n // 2, n))]) * 2
+    bad = step(summed)
+    assert np.abs(bad.astype(np.float64) - one.astype(np.float64)).max() > 1e-5
+
+
 # ------------------------------------------------------------------ bf16
 
 def test_bf16_rounding_matches_torch():
