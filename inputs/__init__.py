@@ -149,8 +149,9 @@ def pad_params(P: int, N: int) -> int:
     return (P + q - 1) // q * q
 
 
-# The five workloads.  Hyperparameters left open by the recipe (initial
-# master weights, m, v, step, eps) are chosen as stated in the design doc.
+# The five workloads.  Where a recipe leaves a value open, the choice is:
+# master weights N(0, 0.02) everywhere; m = v = 0 and step 1 unless the recipe
+# fixes them (the 1.5B recipe does); eps 1e-8; rank r's gradients seeded r.
 TINY = Workload("tiny-zero1-n4-p4096", N=4, P=4096, gdtype="f32", wdtype="bf16",
                 grad=Dist(UNIFORM), master=Dist(NORMAL, 0.02), lr=1e-3,
                 beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, step=1, clip=0.0)

@@ -26,7 +26,7 @@ def dpz():
     return d
 
 
-def test_header_declares_the_north_star_calls(dpz):
+def test_header_declares_the_step_calls(dpz):
     names = dpz.header_symbols()
     for n in ("dp_reduce_scatter_avg", "dp_allreduce_avg", "dp_grad_global_norm",
               "zero1_adamw_step", "dp_allgather", "dp_zero1_step", "dpz_workspace_bytes",

@@ -14,7 +14,7 @@ import inputs as I
 from conftest import ROOT
 
 
-def test_step_bytes_match_the_survey_table():
+def test_step_bytes_match_the_minimal_traffic_formula():
     # N*P*e_g + 24*P + N*P*e_w: 40P for N = 4 bf16, 56P for N = 8 bf16
     assert bench.step_bytes(I.GPT2_1P5B) == 40 * 1_557_611_200 == 62_304_448_000
     assert bench.step_bytes(I.GPT2_124M) == 56 * 124_439_808
