@@ -81,6 +81,14 @@ def test_zero1_step_full_size(w, acc32):
     dpz.dp_zero1_step(G, T, M, V, W, N, cfg, ws=ws, norm_out=nrm, acc32=acc32)
     torch.cuda.synchronize()
     gnorm = nrm.item()
+    # the standalone norm (bulk-copy staged kernel) of the stored averages is
+    # the same float: the same per-segment partials, summed in the same order
+    ws2, nrm2 = dpz.workspace(P, N, DEV), torch.zeros(1, device=DEV)
+    dpz.dp_grad_global_norm(G, N, ws2, nrm2)
+    torch.cuda.synchronize()
+    assert nrm2.item() == gnorm
+    assert dpz.device_status() == 0
+    del ws2
 
     ss = oracle_full_sumsq(w, acc32=acc32)
     onorm, oscale = O.clip_scale(ss, w.clip)
