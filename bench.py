@@ -243,18 +243,26 @@ def time_oracle(w: I.Workload, seconds: float) -> dict:
                       f"of {w.name} ({elapsed:.1f} s single-threaded)"}
 
 
-def time_oracle_threads(w: I.Workload, seconds: float, threads: int) -> dict:
+def oracle_thread_windows(w: I.Workload, threads: int) -> list:
+    """Inputs of `threads` disjoint windows of the workload, one per thread."""
+    width = min(w.C, 1 << 18)
+    span = max(1, (w.C - width) // max(1, threads))
+    return [oracle_window_step(w, width, offset=min(w.C - width, t * span) // 8 * 8)
+            for t in range(threads)]
+
+
+def time_oracle_threads(w: I.Workload, seconds: float, threads: int, bases=None) -> dict:
     """The same oracle, unchanged, on `threads` disjoint windows of the
     workload at once, one host thread each (the oracle's C calls release the
-    GIL), for about `seconds` of wall time; throughput in the metric's unit."""
+    GIL), for about `seconds` of wall time; throughput in the metric's unit.
+    `bases`: the windows' inputs from oracle_thread_windows, to reuse."""
     import threading
     import oracle as O
     width = min(w.C, 1 << 18)
     cfg = O.cfg_from_workload(w)
     mini = w.with_(P=w.N * width)
-    span = max(1, (w.C - width) // max(1, threads))
-    bases = [oracle_window_step(w, width, offset=min(w.C - width, t * span) // 8 * 8)
-             for t in range(threads)]
+    if bases is None:
+        bases = oracle_thread_windows(w, threads)
     counts = [0] * threads
     start = threading.Barrier(threads + 1)
     stop = threading.Event()
@@ -288,15 +296,18 @@ def time_oracle_threads(w: I.Workload, seconds: float, threads: int) -> dict:
 
 
 def run_reference(args) -> None:
-    """The CPU oracle timed as the reference arm: rank 0 only, each step a
-    bounded window of the workload, the whole run kept to a few minutes."""
+    """The CPU oracle timed as the reference arm: rank 0 only, the unchanged
+    oracle on disjoint windows of the workload, one per host core, each step a
+    bounded slice of wall time, the whole run kept to a few minutes."""
     if int(os.environ.get("RANK", "0")) != 0:
         return
     w = I.WORKLOADS[args.workload]
+    threads = os.cpu_count() or 1
+    bases = oracle_thread_windows(w, threads)
     per_step = []
     secs = min(args.ref_seconds, 150.0 / max(1, args.warmup + args.steps))
     for i in range(args.warmup + args.steps):
-        r = time_oracle(w, secs)
+        r = time_oracle_threads(w, secs, threads, bases)
         if i >= args.warmup:
             per_step.append(r)
     vals = [r["value"] for r in per_step]
@@ -307,7 +318,7 @@ def run_reference(args) -> None:
             "steps_per_s": value * 1e9 / step_bytes(w),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": config_of(w),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": per_step[-1]["sample"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
