@@ -183,6 +183,8 @@ def dist_setup(gpus: int):
         import torch.distributed as dist
         import torch
         backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)      # each rank's collectives on its own GPU
         dist.init_process_group(backend)
     return world, rank, local
 
