@@ -370,6 +370,20 @@ def test_adamw_first_step_closed_form(golden):
     assert np.all(np.abs(th.astype(np.float64) - rows[:, 2]) <= tol)
 
 
+def test_adamw_closed_form_fixture_is_its_script_output():
+    """The stored closed-form values are what the committed generator writes
+    (exact rational arithmetic, no oracle, no CUDA)."""
+    import importlib.util
+    import os
+    from conftest import GOLDEN
+    path = os.path.join(GOLDEN, "make_adamw_t1_closed_form.py")
+    spec = importlib.util.spec_from_file_location("_make_adamw_t1", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    with open(os.path.join(GOLDEN, "adamw_t1_closed_form.txt")) as f:
+        assert f.read().splitlines() == mod.lines()
+
+
 def test_adamw_first_step_closed_form_random():
     rng = np.random.default_rng(5)
     n = 4096
