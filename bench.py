@@ -327,13 +327,31 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+L2_BYTES = 129e6
+
+
+def touched_bytes(w: I.Workload) -> int:
+    """Device bytes one step reads or writes: the gradient arena for an
+    all-reduce; gradients, weights and master/m/v for the step."""
+    if w.allreduce_only:
+        return w.N * w.P * w.grad_bytes()
+    return w.N * w.P * (w.grad_bytes() + w.weight_bytes()) + 12 * w.P
+
+
+def l2_note(w: I.Workload) -> str:
+    b = touched_bytes(w)
+    if b > 2 * L2_BYTES:
+        return "inputs larger than L2 (%.2f GB touched per step vs 129 MB L2)" % (b / 1e9)
+    return ("arena within reach of L2 (%.1f MB touched per step vs 129 MB L2): no flush "
+            "between steps, so the figures include L2 reuse" % (b / 1e6))
+
+
 def config_of(w: I.Workload, acc32: bool = False) -> dict:
     c = {"workload": w.name, "ranks_simulated": w.N, "P": w.P,
          "grad_dtype": w.gdtype + ("+fp32-accumulate" if acc32 else ""),
          "weight_dtype": w.wdtype, "state_dtype": "f32" if not w.allreduce_only else None,
          "clip": w.clip, "step_t": w.step,
-         "l2": "inputs larger than L2 (resident arena %.1f GB vs 129 MB L2)" % (
-             (w.N * w.P * (w.grad_bytes() + w.weight_bytes()) + 12 * w.P) / 1e9),
+         "l2": l2_note(w),
          "parallelism": f"{w.N} simulated ranks per GPU"}
     return c
 
