@@ -811,7 +811,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["dpz", "reference"], default="dpz")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--e2e-buckets", type=int, default=0,
                     help="> 1: pipeline the e2e host copies with bucketed reduce-scatters")
     ap.add_argument("--entry", choices=ENTRIES, default="step",
