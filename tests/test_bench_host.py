@@ -85,3 +85,12 @@ def test_cpu_baselines_single_and_threaded():
     for r, cores in ((one, 1), (many, 2)):
         assert r["kind"] == "oracle" and r["unit"] == bench.UNIT and r["cores"] == cores
         assert r["value"] > 0 and "windows" in r["sample"]
+
+
+def test_l2_note_says_which_workloads_stream_from_hbm():
+    assert bench.l2_note(I.GPT2_1P5B).startswith("inputs larger than L2")
+    assert bench.l2_note(I.ALLREDUCE_7B).startswith("inputs larger than L2")
+    assert bench.touched_bytes(I.ALLREDUCE_7B) == 4 * 7_000_000_000 * 2
+    assert "L2 reuse" in bench.l2_note(I.TINY)
+    assert "L2 reuse" in bench.l2_note(I.allreduce_sweep(16 << 20, 4))     # 64 MiB arena
+    assert bench.l2_note(I.allreduce_sweep(1 << 30, 2)).startswith("inputs larger than L2")
