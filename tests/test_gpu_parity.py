@@ -256,6 +256,35 @@ def test_clip_boundary(N, C):
     check_step(below, g, th, m, v, wts, out2)
 
 
+def _random_cases(n_cases, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n_cases):
+        N = int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 11, 16]))
+        C = 8 * int(rng.integers(1, 750))                      # 8 .. 5,992 elements
+        gdt, wdt = [("bf16", "bf16"), ("f32", "bf16"), ("f32", "f32"), ("bf16", "f32")][
+            int(rng.integers(0, 4))]
+        clip = float(rng.choice([0.0, 1e-3]))
+        acc32 = gdt == "bf16" and bool(rng.integers(0, 2))
+        cases.append((N, C, gdt, wdt, clip, acc32, int(rng.integers(0, 1 << 30))))
+    return cases
+
+
+@pytest.mark.parametrize("N,C,gdt,wdt,clip,acc32,seed", _random_cases(32, 2026))
+def test_random_shapes(N, C, gdt, wdt, clip, acc32, seed):
+    """Seeded random shapes (N up to 16, chunks of 8 to 5,992 elements, so
+    segments, tiles and the small-arena path all meet ragged ends), dtype
+    pairs, clip and the fp32-accumulating ring: the fused step against the
+    oracle, and against the four separate calls bit for bit."""
+    w, g, th, m, v, wts = make_problem(N, C, gdt, wdt, clip, seed=seed)
+    a = run_gpu_step(w, g, th, m, v, wts, fused=True, acc32=acc32)
+    check_step(w, g, th, m, v, wts, a, acc32=acc32)
+    b = run_gpu_step(w, g, th, m, v, wts, fused=False, acc32=acc32)
+    for x, y in zip(a[:5], b[:5]):
+        assert same_bits(x, y)
+    assert a[5] == b[5]
+
+
 def test_deterministic():
     w, g, th, m, v, wts = make_problem(8, 12344, "bf16", "bf16", 1e-3, seed=1)
     a = run_gpu_step(w, g, th, m, v, wts)
