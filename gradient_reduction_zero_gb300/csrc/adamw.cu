@@ -208,6 +208,9 @@ static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, A
                             int64_t avg_stride)
 {
     if (src == AdamSrc::kFold) {
+        if (zero1_fused_staged(a))   // staged through shared memory by bulk copies (staged.cu)
+            return launch_zero1_fused_tma(a, avg, h, store_avg, grads, master, m, v, weights, ws,
+                                          s);
         if (ws != nullptr)
             return fused_n<GDT, WDT, true>(a, avg, h, store_avg, grads, master, m, v, weights, ws,
                                            s);

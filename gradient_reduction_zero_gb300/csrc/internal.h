@@ -119,6 +119,13 @@ cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h
 cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
                                    int64_t avg_stride, float* master, float* m, float* v,
                                    void* weights, const void* ws, cudaStream_t s);
+// The step without clip, staged the same way, for N in {1, 2, 4, 8}
+// (zero1_fused_staged); other N use k_adamw's fold.  ws: norm partials when
+// not NULL.
+bool zero1_fused_staged(const Arena& a);
+cudaError_t launch_zero1_fused_tma(const Arena& a, const Avg& avg, const AdamArgs& h,
+                                   bool store_avg, void* grads, float* master, float* m, float* v,
+                                   void* weights, void* ws, cudaStream_t s);
 cudaError_t read_and_clear_pipeline_error(unsigned* flag);
 // Launch the staged AdamW kernel on a one-tile arena in `buf` (256 bytes)
 // with a barrier that never completes, so that its bounded wait runs out.

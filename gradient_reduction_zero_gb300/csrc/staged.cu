@@ -8,6 +8,10 @@
 //   bulk-stores master/m/v and the cast weights into the N weight slabs and
 //   waits until those stores have read shared memory.  The arithmetic is
 //   adamw_elem, so the results are bit-identical to k_adamw.
+// - The whole step without clip (ring fold of the N slabs, average, AdamW,
+//   cast, N weight stores, optional averages store and norm partials), for
+//   compile-time N: one 1024-element tile of every slab plus master/m/v per
+//   128-thread CTA, the same load / update / store shape.
 // - Sums of squares of the owner chunks (the standalone norm): one 32 KB tile
 //   per 256-thread CTA, one bulk load, then each warp takes segments of the
 //   tile.  Large tiles keep ~220 KB of loads in flight per SM, which a
@@ -149,6 +153,118 @@ k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __r
     }
 }
 
+// ------------------------------------------------------------ fold step
+
+template <int GDT, int WDT, int NT>
+struct FoldTile {
+    unsigned char g[NT][kTmaTile * Group<GDT>::kBytes];   // slab r's tile at g[r]
+    float th[kTmaTile];
+    float m[kTmaTile];
+    float v[kTmaTile];
+    unsigned char w[kTmaTile * Group<WDT>::kBytes];
+};
+
+// The step without clip for N == NT: every lane folds its 8 elements over the
+// NT slab tiles in ring order (fold_loaded, the same arithmetic as k_adamw),
+// averages, adds its sum of squares to its warp's segment partial (a warp
+// covers one 256-element segment of the tile), runs AdamW and casts.  With
+// store_avg the averages replace slab c's tile and are stored into slab c.
+template <int GDT, int WDT, int NT, bool SUMSQ>
+__global__ void __launch_bounds__(kTmaThreads)
+k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
+                  float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C,
+                  Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
+                  double* __restrict__ partials)
+{
+    using GS = Group<GDT>;
+    using WS = Group<WDT>;
+    constexpr int GES = GS::kBytes;
+    constexpr int WES = WS::kBytes;
+    extern __shared__ __align__(128) unsigned char dsmem[];
+    FoldTile<GDT, WDT, NT>& t = *reinterpret_cast<FoldTile<GDT, WDT, NT>*>(dsmem);
+    __shared__ __align__(8) uint64_t full;
+    __shared__ int timed_out;
+
+    const int64_t tiles_per_chunk = (C + kTmaTile - 1) / kTmaTile;
+    const int c = (int)(blockIdx.x / tiles_per_chunk);
+    const int64_t tc = blockIdx.x - (int64_t)c * tiles_per_chunk;
+    const int64_t e = (int64_t)c * C + tc * kTmaTile;
+    const int64_t left = C - tc * kTmaTile;
+    const int n = (int)(left < kTmaTile ? left : kTmaTile);   // a multiple of 8
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int64_t gslab = P * GES;
+
+    if (SUMSQ && blockIdx.x == 0 && tid == 0) hdr->arrive = 0u;
+    if (tid == 0) {
+        mbar_init_one(&full);
+        timed_out = 0;
+        mbar_expect_tx(&full, (uint32_t)n * (NT * GES + 12u));
+#pragma unroll
+        for (int r = 0; r < NT; ++r)
+            bulk_load(t.g[r], grads + r * gslab + e * GES, (uint32_t)n * GES, &full);
+        bulk_load(t.th, master + e, (uint32_t)n * 4u, &full);
+        bulk_load(t.m, mom + e, (uint32_t)n * 4u, &full);
+        bulk_load(t.v, var + e, (uint32_t)n * 4u, &full);
+    }
+    __syncthreads();     // the barrier is initialised before anyone waits on it
+    if (!mbar_wait_bounded(&full)) atomicExch(&timed_out, 1);
+    __syncthreads();
+    if (timed_out) {
+        if (tid == 0) abandon_tile(&full);
+        return;
+    }
+
+    const int i0 = tid * kGroup;
+    float ss = 0.0f;
+    if (i0 < n) {
+        typename GS::Raw raw[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {                   // ring order: slabs c+1, ..., c
+            int r = c + 1 + j;
+            if (r >= NT) r -= NT;
+            raw[j] = *reinterpret_cast<const typename GS::Raw*>(t.g[r] + i0 * GES);
+        }
+        float g[8];
+        fold_loaded<GDT, NT>(raw, g);
+        average8<GDT>(g, avg);
+        if (SUMSQ) ss = sumsq8(g);
+        if (store_avg) *reinterpret_cast<typename GS::Raw*>(t.g[c] + i0 * GES) = GS::pack(g);
+        float th[8], mm[8], vv[8];
+        Group<0>::unpack(*reinterpret_cast<const U8*>(&t.th[i0]), th);
+        Group<0>::unpack(*reinterpret_cast<const U8*>(&t.m[i0]), mm);
+        Group<0>::unpack(*reinterpret_cast<const U8*>(&t.v[i0]), vv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) adamw_elem(th[q], mm[q], vv[q], g[q], h);
+        *reinterpret_cast<U8*>(&t.th[i0]) = Group<0>::pack(th);
+        *reinterpret_cast<U8*>(&t.m[i0]) = Group<0>::pack(mm);
+        *reinterpret_cast<U8*>(&t.v[i0]) = Group<0>::pack(vv);
+        *reinterpret_cast<typename WS::Raw*>(t.w + i0 * WES) = WS::pack(th);
+    }
+    if (SUMSQ) {
+        const float tsum = warp_sum_f32(ss);                // whole warps
+        const int seg = tid >> 5;
+        if (lane == 0 && seg * kSegment < n)
+            partials[c * segments_per_chunk(C) + tc * (kTmaTile / kSegment) + seg] = (double)tsum;
+    }
+    // the threads' shared-memory writes become visible to the bulk stores
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(master + e, t.th, (uint32_t)n * 4u);
+        bulk_store(mom + e, t.m, (uint32_t)n * 4u);
+        bulk_store(var + e, t.v, (uint32_t)n * 4u);
+        const int64_t wslab = P * WES;
+#pragma unroll
+        for (int r = 0; r < NT; ++r)
+            bulk_store(weights + r * wslab + e * WES, t.w, (uint32_t)n * WES);
+        if (store_avg) bulk_store(grads + c * gslab + e * GES, t.g[c], (uint32_t)n * GES);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        // shared memory is released when the CTA exits: wait until the stores
+        // have read it (their writes to global memory complete on their own)
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    }
+}
+
 // ------------------------------------------------------------ norm
 
 constexpr int kNormTileBytes = 32768;
@@ -264,10 +380,85 @@ cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void
                                    void* weights, const void* ws, cudaStream_t s)
 {
     const bool gbf = a.gdt != 0;       // stored averages: bf16 in both bf16 modes
-    if (gbf && a.wdt == 1) return tma_n<1, 1>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    if (gbf && a.wdt == 1)
+        return tma_n<1, 1>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     if (gbf) return tma_n<1, 0>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     if (a.wdt == 1) return tma_n<0, 1>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     return tma_n<0, 0>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+}
+
+template <int GDT, int WDT, int NT, bool SUMSQ>
+static cudaError_t fused_tma_t(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
+                               void* grads, float* master, float* m, float* v, void* weights,
+                               void* ws, cudaStream_t s)
+{
+    auto fn = k_zero1_fused_tma<GDT, WDT, NT, SUMSQ>;
+    const size_t smem = sizeof(FoldTile<GDT, WDT, NT>);
+    const cudaError_t e = allow_smem(reinterpret_cast<const void*>(fn), smem);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (a.C + kTmaTile - 1) / kTmaTile * a.N;
+    set_last_kernel_name(SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused");
+    fn<<<(unsigned)tiles, kTmaThreads, smem, s>>>(
+        static_cast<char*>(grads), master, m, v, static_cast<char*>(weights), a.P, a.C, avg, h,
+        store_avg ? 1 : 0, static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr);
+    return cudaGetLastError();
+}
+
+template <int GDT, int WDT, bool SUMSQ>
+static cudaError_t fused_tma_n(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
+                               void* grads, float* master, float* m, float* v, void* weights,
+                               void* ws, cudaStream_t s)
+{
+    switch (a.N) {
+    case 1:
+        return fused_tma_t<GDT, WDT, 1, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                weights, ws, s);
+    case 2:
+        return fused_tma_t<GDT, WDT, 2, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                weights, ws, s);
+    case 4:
+        return fused_tma_t<GDT, WDT, 4, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                weights, ws, s);
+    default:
+        return fused_tma_t<GDT, WDT, 8, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                weights, ws, s);
+    }
+}
+
+template <int GDT, int WDT>
+static cudaError_t fused_tma_dt(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
+                                void* grads, float* master, float* m, float* v, void* weights,
+                                void* ws, cudaStream_t s)
+{
+    if (ws != nullptr)
+        return fused_tma_n<GDT, WDT, true>(a, avg, h, store_avg, grads, master, m, v, weights,
+                                           ws, s);
+    return fused_tma_n<GDT, WDT, false>(a, avg, h, store_avg, grads, master, m, v, weights, ws,
+                                        s);
+}
+
+bool zero1_fused_staged(const Arena& a)
+{
+    return a.N == 1 || a.N == 2 || a.N == 4 || a.N == 8;
+}
+
+cudaError_t launch_zero1_fused_tma(const Arena& a, const Avg& avg, const AdamArgs& h,
+                                   bool store_avg, void* grads, float* master, float* m, float* v,
+                                   void* weights, void* ws, cudaStream_t s)
+{
+    if (!zero1_fused_staged(a)) return cudaErrorInvalidValue;
+    const bool wb = a.wdt == 1;
+    switch (a.gdt) {
+    case 0:
+        return wb ? fused_tma_dt<0, 1>(a, avg, h, store_avg, grads, master, m, v, weights, ws, s)
+                  : fused_tma_dt<0, 0>(a, avg, h, store_avg, grads, master, m, v, weights, ws, s);
+    case 1:
+        return wb ? fused_tma_dt<1, 1>(a, avg, h, store_avg, grads, master, m, v, weights, ws, s)
+                  : fused_tma_dt<1, 0>(a, avg, h, store_avg, grads, master, m, v, weights, ws, s);
+    default:
+        return wb ? fused_tma_dt<2, 1>(a, avg, h, store_avg, grads, master, m, v, weights, ws, s)
+                  : fused_tma_dt<2, 0>(a, avg, h, store_avg, grads, master, m, v, weights, ws, s);
+    }
 }
 
 template <int GDT>
