@@ -5,9 +5,10 @@
  * A "rank" is a replica slab of an arena.  The collectives of the pages become
  * in-memory kernels: a ring "send" of a chunk is a load from another slab, the
  * ring's hop order is a fixed per-element fold order, and an all-gather is N
- * coalesced stores.  Every call is asynchronous on the caller's CUDA stream,
- * never synchronises the host, allocates nothing, and launches only this
- * library's own kernels.
+ * coalesced stores.  Every compute call is asynchronous on the caller's CUDA
+ * stream, never synchronises the host, allocates nothing, and launches only
+ * this library's own kernels (dpz_device_status, a read of a device flag, is
+ * the one synchronous call).
  *
  * ------------------------------------------------------------------------
  * Layout (all buffers are owned and allocated by the caller, device memory)
@@ -41,19 +42,19 @@
  * Status: every call returns DPZ_OK or an error code without launching
  * anything when an argument is invalid (null pointer, N out of range,
  * P <= 0, P % N != 0, bad dtype, step < 1, overlapping buffers), and
- * DPZ_ERR_ALIGN for misaligned pointers or chunks (P/N not a multiple of 8).  A CUDA launch failure
- * returns DPZ_ERR_CUDA.  dpz_last_error() gives the calling thread's last
- * message.  NaN and Inf inputs are not special-cased: they propagate.
+ * DPZ_ERR_ALIGN for misaligned pointers or chunks (P/N not a multiple of 8).
+ * A CUDA launch failure returns DPZ_ERR_CUDA.  dpz_last_error() gives the
+ * calling thread's last message.  NaN and Inf inputs are not special-cased:
+ * they propagate.
  *
  * Streams: the caller orders producers of `grads` before the call with
  * events (A4 Part 3: record an event on the compute stream, make the
  * communication stream wait on it), and consumers after it.
  *
- * CUDA graphs: dp_reduce_scatter_avg, dp_allreduce_avg, dp_grad_global_norm,
- * zero1_adamw_step, dp_allgather and dp_zero1_step only enqueue kernels on
- * `stream`, so they can be captured into a CUDA graph and replayed.  Call
- * each once outside capture first (its launch configuration is cached per
- * device) and keep profiling off while capturing.
+ * CUDA graphs: every compute call except dp_grad_global_norm_static only
+ * enqueues kernels on `stream`, so it can be captured into a CUDA graph and
+ * replayed.  Call each once outside capture first (its launch configuration
+ * is cached per device) and keep profiling off while capturing.
  */
 #ifndef DPZ_H
 #define DPZ_H
