@@ -177,28 +177,14 @@ static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bo
     return cudaGetLastError();
 }
 
+// The fold kernel for the N that the staged kernel does not take (N > 8).
 template <int GDT, int WDT, bool SUMSQ>
 static cudaError_t fused_n(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
                            void* grads, float* master, float* m, float* v, void* weights,
                            void* ws, cudaStream_t s)
 {
-    switch (a.N) {
-    case 1:
-        return adamw_t<GDT, WDT, 1, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s, a.P);
-    case 2:
-        return adamw_t<GDT, WDT, 2, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s, a.P);
-    case 4:
-        return adamw_t<GDT, WDT, 4, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s, a.P);
-    case 8:
-        return adamw_t<GDT, WDT, 8, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s, a.P);
-    default:
-        return adamw_t<GDT, WDT, 0, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                      weights, ws, s, a.P);
-    }
+    return adamw_t<GDT, WDT, 0, true, true, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                  weights, ws, s, a.P);
 }
 
 template <int GDT, int WDT>

@@ -211,6 +211,17 @@ DPZ_API int dpz_selftest_staged_timeout(void* buf, void* stream)
     return ok();
 }
 
+DPZ_API int dpz_selftest_average_division(int N, unsigned long long* mismatches, void* stream)
+{
+    if (N < 1 || N > DPZ_MAX_RANKS)
+        return fail(DPZ_ERR_INVALID_ARG, "N must be in [1, %d] (got %d)", DPZ_MAX_RANKS, N);
+    DPZ_TRY(check_ptr(mismatches, "mismatches"));
+    cudaStream_t s = as_stream(stream);
+    const Avg avg = make_avg(N);
+    DPZ_TRY(launch(s, [&] { return launch_selftest_division(avg, mismatches, s); }));
+    return ok();
+}
+
 DPZ_API int dpz_device_status(int* flag_out)
 {
     if (flag_out == nullptr) return fail(DPZ_ERR_INVALID_ARG, "flag_out is NULL");

@@ -119,8 +119,10 @@ cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h
 cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
                                    int64_t avg_stride, float* master, float* m, float* v,
                                    void* weights, const void* ws, cudaStream_t s);
-// The step without clip, staged the same way, for N in {1, 2, 4, 8}
-// (zero1_fused_staged); other N use k_adamw's fold.  ws: norm partials when
+// The step without clip, staged the same way (compile-time fold for N <= 8,
+// run-time fold beyond) where zero1_fused_staged holds: N <= 8, or N slab
+// tiles that fit shared memory with enough of them resident per SM to keep
+// the stream going; other arenas use k_adamw's fold.  ws: norm partials when
 // not NULL.
 bool zero1_fused_staged(const Arena& a);
 cudaError_t launch_zero1_fused_tma(const Arena& a, const Avg& avg, const AdamArgs& h,
@@ -130,6 +132,10 @@ cudaError_t read_and_clear_pipeline_error(unsigned* flag);
 // Launch the staged AdamW kernel on a one-tile arena in `buf` (256 bytes)
 // with a barrier that never completes, so that its bounded wait runs out.
 cudaError_t launch_staged_timeout_selftest(void* buf, cudaStream_t s);
+// Counts the float inputs whose average division by N differs from an
+// IEEE division (the whole 2^32 pattern space).
+cudaError_t launch_selftest_division(const Avg& avg, unsigned long long* mismatches,
+                                     cudaStream_t s);
 
 
 // The fixed device scratch of dp_grad_global_norm_static (norm_static.cu):

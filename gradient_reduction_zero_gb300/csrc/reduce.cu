@@ -248,10 +248,14 @@ static cudaError_t reduce_t(const Arena& a, const Avg& avg, void* grads, void* w
 template <int GDT, bool ALL, bool SUMSQ>
 static cudaError_t reduce_n(const Arena& a, const Avg& avg, void* grads, void* ws, cudaStream_t s)
 {
-    switch (a.N) {
+    switch (a.N) {       // compile-time folds for N <= 8, the run-time fold beyond
     case 1: return reduce_t<GDT, 1, ALL, SUMSQ>(a, avg, grads, ws, s);
     case 2: return reduce_t<GDT, 2, ALL, SUMSQ>(a, avg, grads, ws, s);
+    case 3: return reduce_t<GDT, 3, ALL, SUMSQ>(a, avg, grads, ws, s);
     case 4: return reduce_t<GDT, 4, ALL, SUMSQ>(a, avg, grads, ws, s);
+    case 5: return reduce_t<GDT, 5, ALL, SUMSQ>(a, avg, grads, ws, s);
+    case 6: return reduce_t<GDT, 6, ALL, SUMSQ>(a, avg, grads, ws, s);
+    case 7: return reduce_t<GDT, 7, ALL, SUMSQ>(a, avg, grads, ws, s);
     case 8: return reduce_t<GDT, 8, ALL, SUMSQ>(a, avg, grads, ws, s);
     default: return reduce_t<GDT, 0, ALL, SUMSQ>(a, avg, grads, ws, s);
     }
@@ -304,7 +308,11 @@ static cudaError_t range_n(const Arena& a, const Avg& avg, const RangeArgs& g, v
     switch (a.N) {
     case 1: return range_t<GDT, 1, SUMSQ>(a, avg, g, ws, s);
     case 2: return range_t<GDT, 2, SUMSQ>(a, avg, g, ws, s);
+    case 3: return range_t<GDT, 3, SUMSQ>(a, avg, g, ws, s);
     case 4: return range_t<GDT, 4, SUMSQ>(a, avg, g, ws, s);
+    case 5: return range_t<GDT, 5, SUMSQ>(a, avg, g, ws, s);
+    case 6: return range_t<GDT, 6, SUMSQ>(a, avg, g, ws, s);
+    case 7: return range_t<GDT, 7, SUMSQ>(a, avg, g, ws, s);
     case 8: return range_t<GDT, 8, SUMSQ>(a, avg, g, ws, s);
     default: return range_t<GDT, 0, SUMSQ>(a, avg, g, ws, s);
     }
@@ -346,6 +354,67 @@ cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s)
     else
         k_allgather<0><<<blocks_for_segments(nseg, StreamSegs<0>::value), kBlock, 0, s>>>(
             w, a.P, a.C, a.N);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Self-test of the average's division: every float bit pattern a, divided by
+// N through divide8, against __fdiv_rn(a, N).  Each thread takes
+// kDivGroupsPerThread groups of 8 consecutive patterns and divides each group
+// twice: as it stands (the group takes one path as a whole) and as 8 copies of
+// one value (so every value that passes markstein_ok is checked on the fast
+// path, zero and the smallest normals included).  Two NaNs count as equal.
+namespace {
+
+constexpr int kDivGroupsPerThread = 16;
+constexpr uint64_t kDivPatterns = 1ull << 32;
+
+__device__ __forceinline__ bool same_quotient(float got, float want)
+{
+    return __float_as_uint(got) == __float_as_uint(want) || (isnan(got) && isnan(want));
+}
+
+__global__ void __launch_bounds__(kBlock)
+k_selftest_division(Avg avg, unsigned long long* mismatches)
+{
+    const uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    unsigned bad = 0;
+    for (int k = 0; k < kDivGroupsPerThread; ++k) {
+        const uint32_t base = (uint32_t)((t * kDivGroupsPerThread + k) * 8);
+        float x[8], want[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            x[q] = __uint_as_float(base + q);
+            want[q] = __fdiv_rn(x[q], avg.fN);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float s[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s[i] = x[q];
+            divide8(s, avg);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) bad += !same_quotient(s[i], want[q]);
+        }
+        divide8(x, avg);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) bad += !same_quotient(x[q], want[q]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bad += __shfl_down_sync(0xffffffffu, bad, o);
+    if ((threadIdx.x & 31) == 0 && bad != 0) atomicAdd(mismatches, (unsigned long long)bad);
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_division(const Avg& avg, unsigned long long* mismatches,
+                                     cudaStream_t s)
+{
+    cudaError_t e = cudaMemsetAsync(mismatches, 0, sizeof(unsigned long long), s);
+    if (e != cudaSuccess) return e;
+    constexpr uint64_t threads = kDivPatterns / 8 / kDivGroupsPerThread;
+    static_assert(threads % kBlock == 0, "the pattern space splits into whole blocks");
+    k_selftest_division<<<(unsigned)(threads / kBlock), kBlock, 0, s>>>(avg, mismatches);
     return cudaGetLastError();
 }
 

@@ -155,35 +155,47 @@ k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __r
 
 // ------------------------------------------------------------ fold step
 
-template <int GDT, int WDT, int NT>
-struct FoldTile {
-    unsigned char g[NT][kTmaTile * Group<GDT>::kBytes];   // slab r's tile at g[r]
-    float th[kTmaTile];
-    float m[kTmaTile];
-    float v[kTmaTile];
-    unsigned char w[kTmaTile * Group<WDT>::kBytes];
-};
+// Shared memory of one fold tile: the tiles of the nr slabs (slab r's at
+// r * fold_slab_tile(GDT)), then master, m and v (fp32), then the cast weights.
+__host__ __device__ constexpr size_t fold_slab_tile(int GDT) { return (size_t)kTmaTile * (GDT == 0 ? 4 : 2); }
+constexpr size_t fold_tile_bytes(int GDT, int WDT, int nr)
+{
+    return (size_t)nr * fold_slab_tile(GDT) + (size_t)kTmaTile * (12 + (WDT == 0 ? 4 : 2));
+}
 
-// The step without clip for N == NT: every lane folds its 8 elements over the
-// NT slab tiles in ring order (fold_loaded, the same arithmetic as k_adamw),
-// averages, adds its sum of squares to its warp's segment partial (a warp
-// covers one 256-element segment of the tile), runs AdamW and casts.  With
-// store_avg the averages replace slab c's tile and are stored into slab c.
+// Largest fold tile the run-time-N kernel takes: two CTAs still fit an SM's
+// 228 KB (bf16 gradients up to N = 47, fp32 up to N = 23; one more with
+// bf16 weights).
+constexpr size_t kFoldTileMaxBytes = 110 * 1024;
+
+// The step without clip: every lane folds its 8 elements over the slab tiles
+// in ring order (for NT > 0 with fold_loaded, for NT == 0 over the n_rt tiles
+// one at a time; both the same arithmetic as k_adamw), averages, adds its sum
+// of squares to its warp's segment partial (a warp covers one 256-element
+// segment of the tile), runs AdamW and casts.  With store_avg the averages
+// replace slab c's tile and are stored into slab c.
 template <int GDT, int WDT, int NT, bool SUMSQ>
 __global__ void __launch_bounds__(kTmaThreads)
 k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
                   float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C,
-                  Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
+                  int n_rt, Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
                   double* __restrict__ partials)
 {
     using GS = Group<GDT>;
     using WS = Group<WDT>;
     constexpr int GES = GS::kBytes;
     constexpr int WES = WS::kBytes;
+    constexpr size_t kSlabTile = fold_slab_tile(GDT);
     extern __shared__ __align__(128) unsigned char dsmem[];
-    FoldTile<GDT, WDT, NT>& t = *reinterpret_cast<FoldTile<GDT, WDT, NT>*>(dsmem);
     __shared__ __align__(8) uint64_t full;
     __shared__ int timed_out;
+
+    const int nr = NT > 0 ? NT : n_rt;
+    unsigned char* const tg = dsmem;
+    float* const tth = reinterpret_cast<float*>(dsmem + (size_t)nr * kSlabTile);
+    float* const tm = tth + kTmaTile;
+    float* const tv = tm + kTmaTile;
+    unsigned char* const tw = reinterpret_cast<unsigned char*>(tv + kTmaTile);
 
     const int64_t tiles_per_chunk = (C + kTmaTile - 1) / kTmaTile;
     const int c = (int)(blockIdx.x / tiles_per_chunk);
@@ -198,13 +210,13 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
     if (tid == 0) {
         mbar_init_one(&full);
         timed_out = 0;
-        mbar_expect_tx(&full, (uint32_t)n * (NT * GES + 12u));
+        mbar_expect_tx(&full, (uint32_t)n * ((uint32_t)nr * GES + 12u));
 #pragma unroll
-        for (int r = 0; r < NT; ++r)
-            bulk_load(t.g[r], grads + r * gslab + e * GES, (uint32_t)n * GES, &full);
-        bulk_load(t.th, master + e, (uint32_t)n * 4u, &full);
-        bulk_load(t.m, mom + e, (uint32_t)n * 4u, &full);
-        bulk_load(t.v, var + e, (uint32_t)n * 4u, &full);
+        for (int r = 0; r < nr; ++r)
+            bulk_load(tg + r * kSlabTile, grads + r * gslab + e * GES, (uint32_t)n * GES, &full);
+        bulk_load(tth, master + e, (uint32_t)n * 4u, &full);
+        bulk_load(tm, mom + e, (uint32_t)n * 4u, &full);
+        bulk_load(tv, var + e, (uint32_t)n * 4u, &full);
     }
     __syncthreads();     // the barrier is initialised before anyone waits on it
     if (!mbar_wait_bounded(&full)) atomicExch(&timed_out, 1);
@@ -217,28 +229,45 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
     const int i0 = tid * kGroup;
     float ss = 0.0f;
     if (i0 < n) {
-        typename GS::Raw raw[NT];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {                   // ring order: slabs c+1, ..., c
-            int r = c + 1 + j;
-            if (r >= NT) r -= NT;
-            raw[j] = *reinterpret_cast<const typename GS::Raw*>(t.g[r] + i0 * GES);
-        }
+        const unsigned char* const gi = tg + i0 * GES;   // this lane's group in slab 0's tile
         float g[8];
-        fold_loaded<GDT, NT>(raw, g);
+        if constexpr (NT > 0) {
+            typename GS::Raw raw[NT];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {               // ring order: slabs c+1, ..., c
+                int r = c + 1 + j;
+                if (r >= NT) r -= NT;
+                raw[j] = *reinterpret_cast<const typename GS::Raw*>(gi + r * kSlabTile);
+            }
+            fold_loaded<GDT, NT>(raw, g);
+        } else {
+            int r = c + 1;
+            if (r >= nr) r -= nr;
+            GS::unpack(*reinterpret_cast<const typename GS::Raw*>(gi + r * kSlabTile), g);
+            for (int j = 2; j <= nr; ++j) {
+                ++r;
+                if (r >= nr) r -= nr;
+                float x[8];
+                GS::unpack(*reinterpret_cast<const typename GS::Raw*>(gi + r * kSlabTile), x);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) g[q] = __fadd_rn(g[q], x[q]);
+                GS::hop_round8(g);
+            }
+        }
         average8<GDT>(g, avg);
         if (SUMSQ) ss = sumsq8(g);
-        if (store_avg) *reinterpret_cast<typename GS::Raw*>(t.g[c] + i0 * GES) = GS::pack(g);
+        if (store_avg)
+            *reinterpret_cast<typename GS::Raw*>(tg + c * kSlabTile + i0 * GES) = GS::pack(g);
         float th[8], mm[8], vv[8];
-        Group<0>::unpack(*reinterpret_cast<const U8*>(&t.th[i0]), th);
-        Group<0>::unpack(*reinterpret_cast<const U8*>(&t.m[i0]), mm);
-        Group<0>::unpack(*reinterpret_cast<const U8*>(&t.v[i0]), vv);
+        Group<0>::unpack(*reinterpret_cast<const U8*>(&tth[i0]), th);
+        Group<0>::unpack(*reinterpret_cast<const U8*>(&tm[i0]), mm);
+        Group<0>::unpack(*reinterpret_cast<const U8*>(&tv[i0]), vv);
 #pragma unroll
         for (int q = 0; q < 8; ++q) adamw_elem(th[q], mm[q], vv[q], g[q], h);
-        *reinterpret_cast<U8*>(&t.th[i0]) = Group<0>::pack(th);
-        *reinterpret_cast<U8*>(&t.m[i0]) = Group<0>::pack(mm);
-        *reinterpret_cast<U8*>(&t.v[i0]) = Group<0>::pack(vv);
-        *reinterpret_cast<typename WS::Raw*>(t.w + i0 * WES) = WS::pack(th);
+        *reinterpret_cast<U8*>(&tth[i0]) = Group<0>::pack(th);
+        *reinterpret_cast<U8*>(&tm[i0]) = Group<0>::pack(mm);
+        *reinterpret_cast<U8*>(&tv[i0]) = Group<0>::pack(vv);
+        *reinterpret_cast<typename WS::Raw*>(tw + i0 * WES) = WS::pack(th);
     }
     if (SUMSQ) {
         const float tsum = warp_sum_f32(ss);                // whole warps
@@ -250,14 +279,15 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     if (tid == 0) {
-        bulk_store(master + e, t.th, (uint32_t)n * 4u);
-        bulk_store(mom + e, t.m, (uint32_t)n * 4u);
-        bulk_store(var + e, t.v, (uint32_t)n * 4u);
+        bulk_store(master + e, tth, (uint32_t)n * 4u);
+        bulk_store(mom + e, tm, (uint32_t)n * 4u);
+        bulk_store(var + e, tv, (uint32_t)n * 4u);
         const int64_t wslab = P * WES;
 #pragma unroll
-        for (int r = 0; r < NT; ++r)
-            bulk_store(weights + r * wslab + e * WES, t.w, (uint32_t)n * WES);
-        if (store_avg) bulk_store(grads + c * gslab + e * GES, t.g[c], (uint32_t)n * GES);
+        for (int r = 0; r < nr; ++r)
+            bulk_store(weights + r * wslab + e * WES, tw, (uint32_t)n * WES);
+        if (store_avg)
+            bulk_store(grads + c * gslab + e * GES, tg + c * kSlabTile, (uint32_t)n * GES);
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         // shared memory is released when the CTA exits: wait until the stores
         // have read it (their writes to global memory complete on their own)
@@ -367,7 +397,11 @@ cudaError_t tma_n(const Arena& a, const AdamArgs& h, const void* grads, int64_t 
     switch (a.N) {
     case 1: return tma_t<GDT, WDT, 1>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     case 2: return tma_t<GDT, WDT, 2>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    case 3: return tma_t<GDT, WDT, 3>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     case 4: return tma_t<GDT, WDT, 4>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    case 5: return tma_t<GDT, WDT, 5>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    case 6: return tma_t<GDT, WDT, 6>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    case 7: return tma_t<GDT, WDT, 7>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     case 8: return tma_t<GDT, WDT, 8>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     default: return tma_t<GDT, WDT, 0>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
     }
@@ -393,14 +427,16 @@ static cudaError_t fused_tma_t(const Arena& a, const Avg& avg, const AdamArgs& h
                                void* ws, cudaStream_t s)
 {
     auto fn = k_zero1_fused_tma<GDT, WDT, NT, SUMSQ>;
-    const size_t smem = sizeof(FoldTile<GDT, WDT, NT>);
-    const cudaError_t e = allow_smem(reinterpret_cast<const void*>(fn), smem);
+    const size_t smem = fold_tile_bytes(GDT, WDT, NT > 0 ? NT : a.N);
+    // the run-time-N kernel may take any tile up to kFoldTileMaxBytes
+    const cudaError_t e = allow_smem(reinterpret_cast<const void*>(fn),
+                                     NT > 0 ? smem : kFoldTileMaxBytes);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (a.C + kTmaTile - 1) / kTmaTile * a.N;
     set_last_kernel_name(SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused");
     fn<<<(unsigned)tiles, kTmaThreads, smem, s>>>(
-        static_cast<char*>(grads), master, m, v, static_cast<char*>(weights), a.P, a.C, avg, h,
-        store_avg ? 1 : 0, static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr);
+        static_cast<char*>(grads), master, m, v, static_cast<char*>(weights), a.P, a.C, a.N, avg,
+        h, store_avg ? 1 : 0, static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr);
     return cudaGetLastError();
 }
 
@@ -416,11 +452,26 @@ static cudaError_t fused_tma_n(const Arena& a, const Avg& avg, const AdamArgs& h
     case 2:
         return fused_tma_t<GDT, WDT, 2, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
                                                 weights, ws, s);
+    case 3:
+        return fused_tma_t<GDT, WDT, 3, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                weights, ws, s);
     case 4:
         return fused_tma_t<GDT, WDT, 4, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
                                                 weights, ws, s);
-    default:
+    case 5:
+        return fused_tma_t<GDT, WDT, 5, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                weights, ws, s);
+    case 6:
+        return fused_tma_t<GDT, WDT, 6, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                weights, ws, s);
+    case 7:
+        return fused_tma_t<GDT, WDT, 7, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                weights, ws, s);
+    case 8:
         return fused_tma_t<GDT, WDT, 8, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                weights, ws, s);
+    default:
+        return fused_tma_t<GDT, WDT, 0, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
                                                 weights, ws, s);
     }
 }
@@ -437,9 +488,31 @@ static cudaError_t fused_tma_dt(const Arena& a, const Avg& avg, const AdamArgs& 
                                         s);
 }
 
+// Shared memory of an SM (sm_103a), and what each resident CTA costs beyond
+// its tile: the runtime's 1 KB reservation and the kernel's static barrier.
+constexpr size_t kSmemPerSm = 228 * 1024;
+constexpr size_t kCtaSmemOverhead = 1024 + 16;
+
+// Staged tiles resident on one SM when the grid fills it.
+static size_t fold_bytes_resident(size_t tile)
+{
+    return kSmemPerSm / (tile + kCtaSmemOverhead) * tile;
+}
+
+// The staged kernel keeps a stream going only with enough bytes in flight per
+// SM.  Measured on the 1.5B-class arenas without clip: tiles resident at 184
+// KB per SM and more ran at 7.08-7.18 TB/s, ahead of the fold kernel by 3-22
+// %; at 156 KB (two 78 KB tiles, e.g. N = 32 bf16 or N = 16 fp32) the fold
+// kernel was as fast or faster.  So for N > 8 the staged kernel is taken when
+// the resident tiles reach 176 KB.
+constexpr size_t kFoldMinResident = 176 * 1024;
+
 bool zero1_fused_staged(const Arena& a)
 {
-    return a.N == 1 || a.N == 2 || a.N == 4 || a.N == 8;
+    if (a.N < 1) return false;
+    if (a.N <= 8) return true;
+    const size_t tile = fold_tile_bytes(a.gdt == 0 ? 0 : 1, a.wdt, a.N);
+    return tile <= kFoldTileMaxBytes && fold_bytes_resident(tile) >= kFoldMinResident;
 }
 
 cudaError_t launch_zero1_fused_tma(const Arena& a, const Avg& avg, const AdamArgs& h,

@@ -70,6 +70,7 @@ _SIGS = {
     "dpz_launch_count": ([], ctypes.c_int64),
     "dpz_device_status": ([ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
     "dpz_selftest_staged_timeout": ([_VP, _VP], ctypes.c_int),
+    "dpz_selftest_average_division": ([ctypes.c_int, _VP, _VP], ctypes.c_int),
     "dpz_profile_start": ([ctypes.c_int], ctypes.c_int),
     "dpz_profile_stop": ([ctypes.POINTER(KernelStat), ctypes.c_int,
                           ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
@@ -255,6 +256,15 @@ def selftest_staged_timeout(buf, stream=None) -> None:
     if buf.numel() * buf.element_size() < SELFTEST_BUF_BYTES:
         raise ValueError(f"buf must hold at least {SELFTEST_BUF_BYTES} bytes")
     _check(lib.dpz_selftest_staged_timeout(_ptr(buf), _stream_handle(stream)))
+
+
+def selftest_average_division(N: int, counter, stream=None) -> None:
+    """Count, into `counter` (a device int64 tensor of one element), the
+    float inputs whose average division by N differs bit for bit from an
+    IEEE division, over all 2^32 bit patterns; 0 means correctly rounded."""
+    if counter.numel() != 1 or counter.element_size() != 8:
+        raise ValueError("counter must be a one-element 8-byte tensor")
+    _check(lib.dpz_selftest_average_division(int(N), _ptr(counter), _stream_handle(stream)))
 
 
 def version() -> str:

@@ -307,10 +307,28 @@ DPZ_API int dpz_device_status(int* flag_out);
  * so the wait runs out, after about two seconds plus the abandon path's
  * bounded wait.  The kernel then sets the device flag and returns without
  * writing `buf`.  After synchronising, dpz_device_status reports 1 and the
- * context is usable.  Returns DPZ_ERR_INVALID_ARG for a NULL or misaligned
- * buf, DPZ_ERR_CUDA if the launch fails. */
+ * context is usable.  Returns DPZ_ERR_INVALID_ARG for a NULL buf,
+ * DPZ_ERR_ALIGN for one not 16-byte aligned, DPZ_ERR_CUDA if the launch
+ * fails. */
 #define DPZ_SELFTEST_BUF_BYTES 256
 DPZ_API int dpz_selftest_staged_timeout(void* buf, void* stream);
+
+/* Self-test of the division inside the average (no counterpart on the pages,
+ * which fix only that the reduced sum is divided by N).  For N not a power of
+ * two the library divides with Markstein's correction of a reciprocal
+ * product instead of an IEEE division; this call checks that the two agree
+ * for every float.  It sets, on `stream`, the 8-byte device counter
+ * `mismatches` (caller memory, 16-byte aligned) to the number of (pattern,
+ * path) cases, over all 2^32 float bit patterns a, where the library's
+ * quotient a/N differs bit for bit from the IEEE round-to-nearest quotient
+ * (two NaNs count as equal).  Each pattern is checked twice: in a group of
+ * 8 consecutive patterns, as the streaming kernels divide them, and in a
+ * group of 8 copies of itself.  0 means the average is correctly rounded for
+ * this N.  It takes a few milliseconds.  Returns DPZ_ERR_INVALID_ARG for
+ * N outside [1, DPZ_MAX_RANKS] or a NULL pointer, DPZ_ERR_ALIGN for one not 16-byte aligned,
+ * DPZ_ERR_CUDA if the launch fails. */
+DPZ_API int dpz_selftest_average_division(int N, unsigned long long* mismatches,
+                                          void* stream);
 
 /* Number of kernels this library has launched since it was loaded. */
 DPZ_API int64_t dpz_launch_count(void);

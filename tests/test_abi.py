@@ -170,3 +170,11 @@ def test_device_status_rejects_null(dpz):
 def test_selftest_rejects_bad_buffer(dpz):
     assert dpz.lib.dpz_selftest_staged_timeout(None, None) == 1
     assert dpz.lib.dpz_selftest_staged_timeout(A + 8, None) == 2        # misaligned
+
+
+def test_division_selftest_rejects_bad_args(dpz):
+    assert dpz.lib.dpz_selftest_average_division(0, A, None) == 1       # N < 1
+    assert dpz.lib.dpz_selftest_average_division(65, A, None) == 1      # N > DPZ_MAX_RANKS
+    assert dpz.lib.dpz_selftest_average_division(3, None, None) == 1    # NULL
+    assert dpz.lib.dpz_selftest_average_division(3, A + 8, None) == 2   # misaligned
+    assert b"mismatches" in dpz.lib.dpz_last_error()
