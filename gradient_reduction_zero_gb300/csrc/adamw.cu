@@ -55,7 +55,7 @@ __device__ __forceinline__ float adamw_group(char* __restrict__ grads, float* __
         } else {
             ring_fold<GDT>(grads, gslab, e * GES, c, N, g);
         }
-        average8<GDT>(g, avg);
+        average8<GDT, NT>(g, avg);
         if (SUMSQ) ss = sumsq8(g);
         if (store_avg) store_group<GDT>(grads + c * gslab + e * GES, g);
     } else {

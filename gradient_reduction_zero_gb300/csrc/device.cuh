@@ -266,7 +266,7 @@ __device__ __forceinline__ void ring_fold(const char* __restrict__ grads, int64_
 // The theorem excludes underflow and non-finite operands, so a group holding
 // a nonzero value below 1e-30 in magnitude, or one that is not finite, is
 // divided instead; a zero gives q0, the exact signed zero.  An exhaustive
-// comparison with __fdiv_rn over all 2^32 float inputs for every N from 2
+// comparison with __fdiv_rn over all 2^32 float inputs for every N from 1
 // to 64 finds no difference (dpz_selftest_average_division).
 __device__ __forceinline__ bool markstein_ok(float a)
 {
@@ -282,30 +282,36 @@ __device__ __forceinline__ float div_markstein(float a, float fN, float invN)
     return a == 0.0f ? q0 : q1;
 }
 
+// NT > 0: N is known at compile time, and only its path is compiled in (the
+// power-of-two kernels stay free of the correction's registers).
+template <int NT = 0>
 __device__ __forceinline__ void divide8(float x[8], const Avg& avg)
 {
-    if (avg.pow2) {
+    constexpr bool kPow2 = NT > 0 && (NT & (NT - 1)) == 0;
+    if (kPow2 || (NT == 0 && avg.pow2)) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) x[q] = __fmul_rn(x[q], avg.invN);
         return;
     }
-    bool fast = true;
+    if constexpr (!kPow2) {
+        bool fast = true;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) fast &= markstein_ok(x[q]);
-    if (fast) {
+        for (int q = 0; q < 8; ++q) fast &= markstein_ok(x[q]);
+        if (fast) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = div_markstein(x[q], avg.fN, avg.invN);
-    } else {
+            for (int q = 0; q < 8; ++q) x[q] = div_markstein(x[q], avg.fN, avg.invN);
+        } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = __fdiv_rn(x[q], avg.fN);
+            for (int q = 0; q < 8; ++q) x[q] = __fdiv_rn(x[q], avg.fN);
+        }
     }
 }
 
-// R(acc / N) for the 8 elements.
-template <int GDT>
+// R(acc / N) for the 8 elements (NT as for divide8).
+template <int GDT, int NT = 0>
 __device__ __forceinline__ void average8(float acc[8], const Avg& avg)
 {
-    divide8(acc, avg);
+    divide8<NT>(acc, avg);
     Group<GDT>::round8(acc);
 }
 

@@ -65,7 +65,7 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
         } else {
             ring_fold<GDT>(grads, slab, off, c, N, acc);
         }
-        average8<GDT>(acc, avg);
+        average8<GDT, NT>(acc, avg);
         if (SUMSQ) ss = sumsq8(acc);
         const typename G::Raw out = G::pack(acc);
         if (ALL) {
@@ -138,7 +138,7 @@ k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restric
             } else {
                 ring_fold<GDT>(src, sslab, soff, c, N, acc);
             }
-            average8<GDT>(acc, avg);
+            average8<GDT, NT>(acc, avg);
             if (SUMSQ) ss = sumsq8(acc);
             G::store_raw(dst + (c * dst_stride + e) * ES, G::pack(acc));
         }
@@ -359,7 +359,8 @@ cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s)
 
 // ---------------------------------------------------------------------------
 // Self-test of the average's division: every float bit pattern a, divided by
-// N through divide8, against __fdiv_rn(a, N).  Each thread takes
+// N through divide8 (the compile-time instantiation the kernels use for N <= 8,
+// the run-time one beyond), against __fdiv_rn(a, N).  Each thread takes
 // kDivGroupsPerThread groups of 8 consecutive patterns and divides each group
 // twice: as it stands (the group takes one path as a whole) and as 8 copies of
 // one value (so every value that passes markstein_ok is checked on the fast
@@ -374,6 +375,7 @@ __device__ __forceinline__ bool same_quotient(float got, float want)
     return __float_as_uint(got) == __float_as_uint(want) || (isnan(got) && isnan(want));
 }
 
+template <int NT>
 __global__ void __launch_bounds__(kBlock)
 k_selftest_division(Avg avg, unsigned long long* mismatches)
 {
@@ -392,11 +394,11 @@ k_selftest_division(Avg avg, unsigned long long* mismatches)
             float s[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) s[i] = x[q];
-            divide8(s, avg);
+            divide8<NT>(s, avg);
 #pragma unroll
             for (int i = 0; i < 8; ++i) bad += !same_quotient(s[i], want[q]);
         }
-        divide8(x, avg);
+        divide8<NT>(x, avg);
 #pragma unroll
         for (int q = 0; q < 8; ++q) bad += !same_quotient(x[q], want[q]);
     }
@@ -414,7 +416,18 @@ cudaError_t launch_selftest_division(const Avg& avg, unsigned long long* mismatc
     if (e != cudaSuccess) return e;
     constexpr uint64_t threads = kDivPatterns / 8 / kDivGroupsPerThread;
     static_assert(threads % kBlock == 0, "the pattern space splits into whole blocks");
-    k_selftest_division<<<(unsigned)(threads / kBlock), kBlock, 0, s>>>(avg, mismatches);
+    const unsigned blocks = (unsigned)(threads / kBlock);
+    switch ((int)avg.fN) {
+    case 1: k_selftest_division<1><<<blocks, kBlock, 0, s>>>(avg, mismatches); break;
+    case 2: k_selftest_division<2><<<blocks, kBlock, 0, s>>>(avg, mismatches); break;
+    case 3: k_selftest_division<3><<<blocks, kBlock, 0, s>>>(avg, mismatches); break;
+    case 4: k_selftest_division<4><<<blocks, kBlock, 0, s>>>(avg, mismatches); break;
+    case 5: k_selftest_division<5><<<blocks, kBlock, 0, s>>>(avg, mismatches); break;
+    case 6: k_selftest_division<6><<<blocks, kBlock, 0, s>>>(avg, mismatches); break;
+    case 7: k_selftest_division<7><<<blocks, kBlock, 0, s>>>(avg, mismatches); break;
+    case 8: k_selftest_division<8><<<blocks, kBlock, 0, s>>>(avg, mismatches); break;
+    default: k_selftest_division<0><<<blocks, kBlock, 0, s>>>(avg, mismatches); break;
+    }
     return cudaGetLastError();
 }
 

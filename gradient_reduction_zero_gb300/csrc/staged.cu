@@ -254,7 +254,7 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
                 GS::hop_round8(g);
             }
         }
-        average8<GDT>(g, avg);
+        average8<GDT, NT>(g, avg);
         if (SUMSQ) ss = sumsq8(g);
         if (store_avg)
             *reinterpret_cast<typename GS::Raw*>(tg + c * kSlabTile + i0 * GES) = GS::pack(g);
