@@ -129,28 +129,36 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
 // t + 512, ... in order, then block_sum), and its second level only adds that
 // value to zeros.  So the norm has the same bits as the two-kernel path, in
 // one launch instead of two for arenas of at most kSmallStepSegments
-// segments, where launch latency is the cost.
-template <int GDT, int WDT>
+// segments, where launch latency is the cost.  The fold is compiled for N
+// (NT > 0, all N loads in flight at once) up to 8, and the block sums the
+// partials from a shared-memory copy instead of reading back the workspace.
+static_assert(kSmallStepSegments <= kFinalThreads, "one partial per thread at most");
+
+template <int GDT, int WDT, int NT>
 __global__ void __launch_bounds__(kFinalThreads)
 k_zero1_small(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
               float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int N,
               Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
               double* __restrict__ partials, float* __restrict__ norm_out)
 {
+    __shared__ double sp[kSmallStepSegments];
     const int64_t segs = segments_per_chunk(C);
-    const int64_t total = (int64_t)N * segs;
+    const int64_t total = (int64_t)N * segs;        // <= kSmallStepSegments
     const int lane = threadIdx.x & 31;
     for (int64_t sw = threadIdx.x >> 5; sw < total; sw += kFinalThreads / 32) {  // whole warps
         const SegPos p = seg_pos(sw, segs);
-        const float ss = adamw_group<GDT, WDT, 0, true, true, true>(
+        const float ss = adamw_group<GDT, WDT, NT, true, true, true>(
             grads, master, mom, var, weights, P, C, N, p.c, p.seg * 32 + lane, avg, h,
             store_avg, false, 1.0f, P);
         const float t = warp_sum_f32(ss);
-        if (lane == 0) partials[p.c * segs + p.seg] = (double)t;
+        if (lane == 0) {
+            partials[sw] = (double)t;                 // sw = p.c * segs + p.seg
+            sp[sw] = (double)t;
+        }
     }
-    __syncthreads();     // every partial of the block is written and visible
+    __syncthreads();     // every partial of the block is in shared memory
     double v = 0.0;
-    for (int64_t i = threadIdx.x; i < total; i += kFinalThreads) v += partials[i];
+    for (int64_t i = threadIdx.x; i < total; i += kFinalThreads) v += sp[i];
     const double r = block_sum(v);
     if (threadIdx.x == 0) {
         const float nrm = __double2float_rn(__dsqrt_rn(r));
@@ -224,16 +232,29 @@ cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     double* parts = ws_partials(ws);
     const int sa = store_avg ? 1 : 0;
+#define DPZ_SMALL_N(GD, WD, NT)                                                              \
+    k_zero1_small<GD, WD, NT><<<1, kFinalThreads, 0, s>>>(g, master, m, v, w, a.P, a.C, a.N,  \
+                                                          avg, h, sa, hdr, parts, norm_out)
 #define DPZ_SMALL(GD, WD)                                                                      \
-    k_zero1_small<GD, WD><<<1, kFinalThreads, 0, s>>>(g, master, m, v, w, a.P, a.C, a.N, avg, \
-                                                      h, sa, hdr, parts, norm_out)
-    if (a.gdt == 2) {
-        if (a.wdt == 1) DPZ_SMALL(2, 1); else DPZ_SMALL(2, 0);
-    } else if (a.gdt == 1) {
-        if (a.wdt == 1) DPZ_SMALL(1, 1); else DPZ_SMALL(1, 0);
-    } else {
-        if (a.wdt == 1) DPZ_SMALL(0, 1); else DPZ_SMALL(0, 0);
+    switch (a.N) {                                                                             \
+    case 1: DPZ_SMALL_N(GD, WD, 1); break;                                                     \
+    case 2: DPZ_SMALL_N(GD, WD, 2); break;                                                     \
+    case 3: DPZ_SMALL_N(GD, WD, 3); break;                                                     \
+    case 4: DPZ_SMALL_N(GD, WD, 4); break;                                                     \
+    case 5: DPZ_SMALL_N(GD, WD, 5); break;                                                     \
+    case 6: DPZ_SMALL_N(GD, WD, 6); break;                                                     \
+    case 7: DPZ_SMALL_N(GD, WD, 7); break;                                                     \
+    case 8: DPZ_SMALL_N(GD, WD, 8); break;                                                     \
+    default: DPZ_SMALL_N(GD, WD, 0); break;                                                    \
     }
+    if (a.gdt == 2) {
+        if (a.wdt == 1) { DPZ_SMALL(2, 1); } else { DPZ_SMALL(2, 0); }
+    } else if (a.gdt == 1) {
+        if (a.wdt == 1) { DPZ_SMALL(1, 1); } else { DPZ_SMALL(1, 0); }
+    } else {
+        if (a.wdt == 1) { DPZ_SMALL(0, 1); } else { DPZ_SMALL(0, 0); }
+    }
+#undef DPZ_SMALL_N
 #undef DPZ_SMALL
     return cudaGetLastError();
 }
