@@ -41,8 +41,16 @@ METRIC = "ZeRO-1 step GB/s and % of GB300 HBM roofline; steps/s vs CPU oracle"
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = I.GPT2_1P5B.name
 PROFILES = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = [os.path.join(ROOT, "gradient_reduction_zero_gb300", "csrc", f)
-                  for f in ("device.cuh", "bulk.cuh", "reduce.cu", "adamw.cu", "staged.cu", "internal.h")]
+CSRC = os.path.join(ROOT, "gradient_reduction_zero_gb300", "csrc")
+# The translation unit of each kernel whose DRAM traffic profiles/ncu_traffic.json
+# holds: its .cu file and the headers it includes.  The traffic of a kernel is
+# used only while these sources (and the nvcc flags) hash as they did when the
+# counters were taken.
+KERNEL_UNITS = {
+    "dpz_rs_avg_sumsq": ("device.cuh", "internal.h", "reduce.cu"),
+    "dpz_adamw_bcast": ("bulk.cuh", "device.cuh", "internal.h", "staged.cu"),
+    "dpz_zero1_fused_sumsq": ("bulk.cuh", "device.cuh", "internal.h", "staged.cu"),
+}
 
 
 # ------------------------------------------------------------------ bytes
@@ -81,16 +89,19 @@ def peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources with comments and whitespace removed, so that
-    it changes when the code does and not when only a comment does."""
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of one kernel's translation unit (KERNEL_UNITS) with comments and
+    whitespace removed, and of the nvcc flags: it changes when the code does,
+    not when only a comment does."""
+    from gradient_reduction_zero_gb300 import build as B
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in (os.path.join(CSRC, f) for f in KERNEL_UNITS[kernel]):
         with open(p, encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)
         h.update(" ".join(text.split()).encode())
+    h.update(" ".join(f for f in B.NVCC_FLAGS if not f.startswith("-I")).encode())
     return h.hexdigest()[:16]
 
 
@@ -102,10 +113,10 @@ def ncu_traffic(kernel: str, w: I.Workload):
         return None
     with open(path) as f:
         t = json.load(f)
-    if t.get("kernel_source_hash") != kernel_source_hash():
-        return None
     k = t.get("kernels", {}).get(kernel)
-    if not k or (k.get("N"), k.get("gdtype"), k.get("wdtype")) != (w.N, w.gdtype, w.wdtype):
+    if not k or kernel not in KERNEL_UNITS or k.get("source_hash") != kernel_source_hash(kernel):
+        return None
+    if (k.get("N"), k.get("gdtype"), k.get("wdtype")) != (w.N, w.gdtype, w.wdtype):
         return None
     return int(k["dram_bytes_per_element"] * w.P)
 

@@ -94,3 +94,31 @@ def test_l2_note_says_which_workloads_stream_from_hbm():
     assert "L2 reuse" in bench.l2_note(I.TINY)
     assert "L2 reuse" in bench.l2_note(I.allreduce_sweep(16 << 20, 4))     # 64 MiB arena
     assert bench.l2_note(I.allreduce_sweep(1 << 30, 2)).startswith("inputs larger than L2")
+
+
+def test_kernel_traffic_follows_its_own_sources(tmp_path, monkeypatch):
+    """A kernel's ncu traffic is used while its translation unit hashes as it
+    did at capture: a code change in it drops the figure, a comment-only
+    change or a change to another kernel's file does not."""
+    import shutil
+    src = tmp_path / "csrc"
+    shutil.copytree(bench.CSRC, src)
+    monkeypatch.setattr(bench, "CSRC", str(src))
+    w = I.GPT2_1P5B
+    before = {k: bench.kernel_source_hash(k) for k in bench.KERNEL_UNITS}
+    with open(src / "adamw.cu", "a") as f:          # in no unit of the table
+        f.write("\nstatic int unrelated_change = 1;\n")
+    with open(src / "reduce.cu", "a") as f:         # comment only
+        f.write("\n// a remark\n/* and another */\n")
+    assert {k: bench.kernel_source_hash(k) for k in bench.KERNEL_UNITS} == before
+    with open(src / "reduce.cu", "a") as f:         # code: only the reduce unit changes
+        f.write("\nstatic int changed = 2;\n")
+    after = {k: bench.kernel_source_hash(k) for k in bench.KERNEL_UNITS}
+    assert after["dpz_rs_avg_sumsq"] != before["dpz_rs_avg_sumsq"]
+    assert after["dpz_adamw_bcast"] == before["dpz_adamw_bcast"]
+    assert after["dpz_zero1_fused_sumsq"] == before["dpz_zero1_fused_sumsq"]
+    # every kernel of the committed table has a unit and a recorded hash
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        table = json.load(f)
+    assert set(table["kernels"]) == set(bench.KERNEL_UNITS)
+    assert all(len(k["source_hash"]) == 16 for k in table["kernels"].values())
