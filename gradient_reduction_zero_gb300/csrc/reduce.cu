@@ -27,13 +27,26 @@ void set_last_kernel_name(const char* n) { g_last_kernel = n; }
 // squares of its averaged elements (fixed shuffle tree) into that segment's
 // slot, so the partials do not depend on the launch configuration.
 
+// Blocks per SM the reduce kernels are compiled for.  A bf16 lane loads 16
+// bytes per slab, so a warp keeps only N x 512 bytes in flight: at 32
+// registers eight blocks (64 warps) stay resident, which took the N = 3
+// reduce-scatter from 94 to 98 % of the copy peak and left N = 2 and 4-8
+// unchanged.  fp32 lanes load 32 bytes per slab; capping their registers
+// cost 0.3-3 % at N = 3-8, so they keep the compiler's choice, as does the
+// all-reduce, which also stores N slabs.
+template <int GDT, bool ALL>
+struct ReduceBlocksPerSm {
+    static constexpr int value = GDT != 0 && !ALL ? 8 : 1;
+};
+
 // Ring-order reduce + average of every chunk, one segment per warp.
 // ALL = false: chunk c goes to slab c only (reduce-scatter).  ALL = true: to
 // every slab (all-reduce).  SUMSQ: per-segment sums of squares of the
 // averages.  NT > 0: N == NT known at compile time; NT == 0: any N, read from
-// n_rt.
+// n_rt.  With bf16 storage the reduce-scatter variants are held to 32
+// registers (ReduceBlocksPerSm).
 template <int GDT, int NT, bool ALL, bool SUMSQ>
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(kBlock, ReduceBlocksPerSm<GDT, ALL>::value)
 k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
          WsHeader* __restrict__ hdr, double* __restrict__ partials)
 {
@@ -100,7 +113,7 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
 // the segments and their partials are the ones the whole-arena kernels
 // write.
 template <int GDT, int NT, bool SUMSQ>
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(kBlock, ReduceBlocksPerSm<GDT, false>::value)
 k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restrict__ dst,
                int64_t dst_stride, int64_t lo, int64_t hi, int64_t C, int n_rt, int c_first,
                Avg avg, WsHeader* __restrict__ hdr, double* __restrict__ partials)
