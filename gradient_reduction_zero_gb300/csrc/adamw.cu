@@ -16,12 +16,14 @@ namespace dpz {
 // grads + (c*avg_stride + e) elements: avg_stride = P for the owner slabs of
 // the arena, 0 for a compact [P] buffer of gradient shards.
 // One-shot grid, one segment per warp (device.cuh).  Register caps that keep
-// more blocks, hence more loads, in flight: 64 registers (four blocks per SM)
-// wherever that does not spill, which is the load-owner variant and the fold
-// over up to four bf16 slabs; 80 (three blocks) for the other folds.
-template <int GDT, int NT, bool FOLD>
+// more blocks, hence more loads, in flight without spilling: 64 registers
+// (four blocks per SM) for the load-owner variant, 80 (three blocks) for the
+// fold.  The launchers instantiate this kernel with NT == 0 only: the step
+// without clip for N <= 8, and for larger N where its tiles fit, is the
+// staged kernel of staged.cu, and small arenas take k_zero1_small.
+template <bool FOLD>
 struct AdamwBlocksPerSm {
-    static constexpr int value = !FOLD || (GDT != 0 && NT > 0 && NT <= 4) ? 4 : 3;
+    static constexpr int value = FOLD ? 3 : 4;
 };
 
 // The work of one lane: group gi of chunk c (nothing if gi is past the chunk
@@ -88,7 +90,7 @@ __device__ __forceinline__ float adamw_group(char* __restrict__ grads, float* __
 }
 
 template <int GDT, int WDT, int NT, bool FOLD, bool BCAST, bool SUMSQ>
-__global__ void __launch_bounds__(kBlock, AdamwBlocksPerSm<GDT, NT, FOLD>::value)
+__global__ void __launch_bounds__(kBlock, AdamwBlocksPerSm<FOLD>::value)
 k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
         float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int n_rt,
         Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
