@@ -31,12 +31,25 @@ void set_last_kernel_name(const char* n) { g_last_kernel = n; }
 // bytes per slab, so a warp keeps only N x 512 bytes in flight: at 32
 // registers eight blocks (64 warps) stay resident, which took the N = 3
 // reduce-scatter from 94 to 98 % of the copy peak and left N = 2 and 4-8
-// unchanged.  fp32 lanes load 32 bytes per slab; capping their registers
-// cost 0.3-3 % at N = 3-8, so they keep the compiler's choice, as does the
-// all-reduce, which also stores N slabs.
-template <int GDT, bool ALL>
+// unchanged.  fp32 lanes load 32 bytes per slab; capping the compile-time
+// folds cost 0.3-3 % at N = 3-8, so they keep the compiler's choice, as does
+// the all-reduce, which also stores N slabs.  The fp32 run-time fold held 88
+// to 110 registers (two blocks per SM); at 64 (four blocks) it went from 98 to
+// 109 % at N = 12 and from 99 to 108 % at N = 16.
+template <int GDT, int NT, bool ALL>
 struct ReduceBlocksPerSm {
-    static constexpr int value = GDT != 0 && !ALL ? 8 : 1;
+    static constexpr int value = ALL ? 1 : GDT != 0 ? 8 : NT == 0 ? 4 : 1;
+};
+
+// The same for the range kernel, whose extra index arithmetic does not fit
+// 32 registers with bf16 storage at N = 7 and 8 (it spills).  Those get the
+// tightest cap that does not spill, which is also the occupancy they had
+// with no bound: six blocks (40 registers), five (48) for the fp32-accumulating
+// mode at N = 8.
+template <int GDT, int NT>
+struct RangeBlocksPerSm {
+    static constexpr int value = GDT == 0 || NT < 7 ? ReduceBlocksPerSm<GDT, NT, false>::value
+                                 : GDT == 2 && NT == 8 ? 5 : 6;
 };
 
 // Ring-order reduce + average of every chunk, one segment per warp.
@@ -46,7 +59,7 @@ struct ReduceBlocksPerSm {
 // n_rt.  With bf16 storage the reduce-scatter variants are held to 32
 // registers (ReduceBlocksPerSm).
 template <int GDT, int NT, bool ALL, bool SUMSQ>
-__global__ void __launch_bounds__(kBlock, ReduceBlocksPerSm<GDT, ALL>::value)
+__global__ void __launch_bounds__(kBlock, ReduceBlocksPerSm<GDT, NT, ALL>::value)
 k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
          WsHeader* __restrict__ hdr, double* __restrict__ partials)
 {
@@ -113,7 +126,7 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
 // the segments and their partials are the ones the whole-arena kernels
 // write.
 template <int GDT, int NT, bool SUMSQ>
-__global__ void __launch_bounds__(kBlock, ReduceBlocksPerSm<GDT, false>::value)
+__global__ void __launch_bounds__(kBlock, RangeBlocksPerSm<GDT, NT>::value)
 k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restrict__ dst,
                int64_t dst_stride, int64_t lo, int64_t hi, int64_t C, int n_rt, int c_first,
                Avg avg, WsHeader* __restrict__ hdr, double* __restrict__ partials)
