@@ -54,7 +54,8 @@ def fused_reference(w, g, th, m, v, acc32):
     return down(G), down(T), down(M), down(V), down(W), nrm.item()
 
 
-@pytest.mark.parametrize("N,C,nb", [(4, 6152, 7), (8, 2056, 5), (3, 1000, 4), (4, 262_144, 12)])
+@pytest.mark.parametrize("N,C,nb", [(4, 6152, 7), (8, 2056, 5), (3, 1000, 4), (7, 1032, 6),
+                                    (4, 262_144, 12)])
 @pytest.mark.parametrize("clip", [0.0, 1e-3])
 @pytest.mark.parametrize("acc32", [False, True])
 @pytest.mark.parametrize("max_ctas", [0, 1, 152])
@@ -156,3 +157,37 @@ def test_range_without_partials_any_alignment():
     for c in range(N):
         sl = slice(c * C, (c + 1) * C)
         assert same_bits(out[c, sl], a[c, sl])
+
+
+@pytest.mark.parametrize("N,C,gdt,acc32", [(7, 1032, "bf16", False), (7, 1032, "bf16", True),
+                                           (8, 776, "bf16", True), (12, 520, "bf16", False),
+                                           (5, 2000, "f32", False), (8, 776, "f32", False),
+                                           (12, 520, "f32", False), (16, 264, "f32", False)])
+def test_range_partials_match_whole_arena(N, C, gdt, acc32):
+    """Every register bound of the range kernel (compile-time N up to 8, the
+    run-time fold beyond, both storage dtypes, fp32 accumulation): the ranges'
+    averages are the oracle's, bit for bit, and the norm from their partials
+    equals the norm of the whole-arena reduce."""
+    w = I.TINY.with_(N=N, P=N * C, gdtype=gdt, grad=I.Dist(I.NORMAL, 1e-3), grad_seed=N + C)
+    g = I.arena_host(w)
+    P = w.P
+    G = up(g)
+    ws = dpz.workspace(P, N, DEV)
+    for lo, n in segment_buckets(P, N, 5, seed=N):
+        dpz.dp_reduce_scatter_avg_range(G, N, lo, n, ws=ws, acc32=acc32)
+    nrm = torch.zeros(1, device=DEV)
+    dpz.dp_grad_norm_finalize(ws, P, N, nrm)
+    G2 = up(g)
+    ws2 = dpz.workspace(P, N, DEV)
+    nrm2 = torch.zeros(1, device=DEV)
+    dpz.dp_reduce_scatter_avg(G2, N, acc32=acc32)
+    dpz.dp_grad_global_norm(G2, N, ws2, nrm2)
+    torch.cuda.synchronize()
+    a = g.copy()
+    O.reduce_scatter_avg(a, acc32=acc32)
+    out, out2 = down(G).reshape(N, P), down(G2).reshape(N, P)
+    for c in range(N):
+        sl = slice(c * C, (c + 1) * C)
+        assert same_bits(out[c, sl], a[c, sl])
+        assert same_bits(out2[c, sl], a[c, sl])
+    assert nrm.item() == nrm2.item() and nrm.item() > 0
