@@ -1,9 +1,9 @@
-"""The average divides the reduced sum by N (ZeRO, Section 5: each rank's
-shard of the gradient is the average over the N ranks).  For N not a power of
-two the kernels divide with Markstein's correction of a reciprocal product;
-this checks, through the library's own division routine, that the quotient
-equals the IEEE round-to-nearest quotient for every one of the 2^32 float bit
-patterns and every N the library accepts (1 to 64)."""
+"""The average divides the reduced sum by N ("Lab 09 — Parallelism, simulated",
+§2: sum, then divide by N).  For N not a power of two the kernels divide with
+Markstein's correction of a reciprocal product; this checks,
+through the library's own division routine, that the quotient equals the IEEE
+round-to-nearest quotient for every one of the 2^32 float bit patterns and
+every N the library accepts (1 to 64)."""
 import pytest
 import torch
 
@@ -23,3 +23,4 @@ def test_average_division_is_correctly_rounded_for_every_float():
     torch.cuda.synchronize()
     bad = {N: int(c) for N, c in zip(NS, counters[:, 0].tolist()) if c != 0}
     assert bad == {}, bad
+
