@@ -227,9 +227,9 @@ DPZ_API int dp_reduce_scatter_avg_range(void* grads, int64_t P, int N, int gdtyp
                                         int64_t lo, int64_t n, void* ws, int max_ctas,
                                         void* stream);
 
-/* ZeRO-2: gradients are sharded too ("Lab 09", §4: stage 2 shards the
- * gradients, 2Ψ + 14Ψ/N bytes per rank; "Distributed training":
- * ZeroSharded[M, N, 2]).  Reduce + average a bucket of N ranks' gradients for
+/* ZeRO-2: gradients are sharded too ("Lab 09 — Parallelism, simulated", §4:
+ * stage 2 shards the gradients, 2Ψ + 14Ψ/N bytes per rank; "Distributed
+ * training": ZeroSharded[M, N, 2]).  Reduce + average a bucket of N ranks' gradients for
  * arena elements [lo, lo+n), held in a staging buffer [N][n] (rank r's
  * values at staging + r*n), into `shards` [P]: the average of element e is
  * written at shards[e], which belongs to rank e / C's shard.  The staging

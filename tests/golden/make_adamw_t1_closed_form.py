@@ -5,7 +5,7 @@ At t = 1 the bias-corrected moments are m_hat = g and v_hat = g*g, so with
 decoupled weight decay scaled by lr the step is
     theta_1 = theta_0 - lr * (g / (|g| + eps) + wd * theta_0)
 for lr = 1e-3, eps = 1e-8, wd = 0.1 (beta1 and beta2 cancel at t = 1).
-Reading of "A4 - Multi-GPU with NCCL and ZeRO-1", Part 4 (AdamW on the owned
+Reading of "A4 — Multi-GPU with NCCL and ZeRO-1", Part 4 (AdamW on the owned
 shard); the hyperparameters are the tiny workload's.
 
     python tests/golden/make_adamw_t1_closed_form.py > tests/golden/adamw_t1_closed_form.txt
@@ -26,7 +26,7 @@ def lines() -> list[str]:
         "# m_hat = g and v_hat = g*g), decoupled weight decay scaled by lr:",
         "#   theta_1 = theta_0 - lr * ( g / (|g| + eps) + wd * theta_0 )",
         "# lr = 1e-3, eps = 1e-8, wd = 0.1 (beta1 = 0.9, beta2 = 0.999 cancel at t = 1),",
-        "# evaluated exactly by make_adamw_t1_closed_form.py.  Readings: \"A4 - Multi-GPU",
+        "# evaluated exactly by make_adamw_t1_closed_form.py.  Readings: \"A4 — Multi-GPU",
         "# with NCCL and ZeRO-1\", Part 4 (AdamW on the owned shard); hyperparameters of",
         "# the tiny workload.",
         "# theta_0 g theta_1",
