@@ -129,12 +129,13 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
 // w + 16, ... of the list; then the block adds the segment partials exactly
 // as k_norm_finalize does when it runs as one block (lane t adds partials t,
 // t + 512, ... in order, then block_sum), and its second level only adds that
-// value to zeros.  So the norm has the same bits as the two-kernel path, in
-// one launch instead of two for arenas of at most kSmallStepSegments
-// segments, where launch latency is the cost.  The fold is compiled for N
-// (NT > 0, all N loads in flight at once) up to 8, and the block sums the
-// partials from a shared-memory copy instead of reading back the workspace.
-static_assert(kSmallStepSegments <= kFinalThreads, "one partial per thread at most");
+// value to zeros (so warp 0's sum alone is taken).  So the norm has the same
+// bits as the two-kernel path, in one launch instead of two for arenas of at
+// most kSmallStepSegments segments, where launch latency is the cost.  The
+// fold is compiled for N (NT > 0, all N loads in flight at once) up to 8, and
+// warp 0 sums the partials from a shared-memory copy instead of reading back
+// the workspace.
+static_assert(kSmallStepSegments <= 32, "every partial is held by warp 0");
 
 template <int GDT, int WDT, int NT>
 __global__ void __launch_bounds__(kFinalThreads)
@@ -159,9 +160,13 @@ k_zero1_small(char* __restrict__ grads, float* __restrict__ master, float* __res
         }
     }
     __syncthreads();     // every partial of the block is in shared memory
-    double v = 0.0;
-    for (int64_t i = threadIdx.x; i < total; i += kFinalThreads) v += sp[i];
-    const double r = block_sum(v);
+    // k_norm_finalize as one block: thread t holds 0 + partial t (t < total,
+    // else 0), block_sum adds them with warp_sum in each warp and then adds the
+    // warp sums with warp_sum again.  With total <= 32 every partial sits in
+    // warp 0, the other warps' sums are +0, and adding +0 to a sum of squares
+    // leaves it unchanged, so warp 0's warp_sum alone has the same bits.
+    if (threadIdx.x >= 32) return;
+    const double r = warp_sum(threadIdx.x < total ? 0.0 + sp[threadIdx.x] : 0.0);
     if (threadIdx.x == 0) {
         const float nrm = __double2float_rn(__dsqrt_rn(r));
         hdr->sumsq = r;
