@@ -35,10 +35,12 @@ void set_last_kernel_name(const char* n) { g_last_kernel = n; }
 // folds cost 0.3-3 % at N = 3-8, so they keep the compiler's choice, as does
 // the all-reduce, which also stores N slabs.  The fp32 run-time fold held 88
 // to 110 registers (two blocks per SM); at 64 (four blocks) it went from 98 to
-// 109 % at N = 12 and from 99 to 108 % at N = 16.
+// 109 % at N = 12 and from 99 to 108 % at N = 16.  bf16 at N = 2 takes two
+// segments per warp (ReduceSegsPerWarp), which does not fit 32 registers: six
+// blocks of 40.
 template <int GDT, int NT, bool ALL>
 struct ReduceBlocksPerSm {
-    static constexpr int value = ALL ? 1 : GDT != 0 ? 8 : NT == 0 ? 4 : 1;
+    static constexpr int value = ALL ? 1 : GDT != 0 ? (NT == 2 ? 6 : 8) : NT == 0 ? 4 : 1;
 };
 
 // The same for the range kernel, whose extra index arithmetic does not fit
@@ -58,6 +60,81 @@ struct RangeBlocksPerSm {
 // averages.  NT > 0: N == NT known at compile time; NT == 0: any N, read from
 // n_rt.  With bf16 storage the reduce-scatter variants are held to 32
 // registers (ReduceBlocksPerSm).
+// Segments per warp of the reduce kernel.  A bf16 lane loads 16 bytes per
+// slab, so at N <= 2 one segment per warp keeps too few bytes in flight:
+// each warp then takes two consecutive segments of the list and issues all
+// their loads before the first add.  On the 1.5B arena that took the
+// reduce-scatter from 85.7 to 97.6 % of the copy peak at N = 1 and from 100.4
+// to 106.1 % at N = 2, and the all-reduce at N = 1 from 6.51 to 7.10 TB/s.
+// The all-reduce at N = 2 did not change, and the reduce-scatter at N = 3
+// fell from 98.0 to 94.2 % (two segments need 48 registers, five blocks),
+// so both keep one segment per warp.
+template <int GDT, int NT, bool ALL>
+struct ReduceSegsPerWarp {
+    static constexpr int value = GDT != 0 && (NT == 1 || (NT == 2 && !ALL)) ? 2 : 1;
+};
+
+// k_reduce's work for SPW > 1 (compile-time N): warp w takes segments
+// w*SPW ... w*SPW + SPW-1 of the chunk-major list.  Each segment is folded,
+// averaged, stored and summed exactly as with one segment per warp.
+template <int GDT, int NT, bool ALL, bool SUMSQ, int SPW>
+__device__ __forceinline__ void reduce_segments(char* __restrict__ grads, int64_t slab, int64_t C,
+                                                int64_t groups, int64_t segs, const Avg& avg,
+                                                double* __restrict__ partials, int lane)
+{
+    static_assert(NT > 0, "several segments per warp need a compile-time N");
+    using G = Group<GDT>;
+    constexpr int ES = G::kBytes;
+    const int64_t total = (int64_t)NT * segs;
+    const int64_t sw0 = global_warp() * SPW;
+    if (sw0 >= total) return;                            // whole warps
+    SegPos ps[SPW];
+    ps[0] = seg_pos(sw0, segs);
+#pragma unroll
+    for (int u = 1; u < SPW; ++u) {
+        ps[u] = ps[u - 1];
+        seg_next(ps[u], segs);
+        if (sw0 + u >= total) ps[u] = ps[0];             // past the list: a slot left idle
+    }
+    const char* src[SPW][NT];
+    typename G::Raw raw[SPW][NT];
+    int64_t off[SPW];
+    bool live[SPW];
+#pragma unroll
+    for (int u = 0; u < SPW; ++u) {                      // every load first
+        const int64_t gi = ps[u].seg * 32 + lane;
+        live[u] = sw0 + u < total && gi < groups;
+        off[u] = (ps[u].c * C + gi * kGroup) * ES;
+        ring_sources<NT>(grads, slab, ps[u].c, src[u]);
+        if (live[u]) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) raw[u][j] = G::load_raw(src[u][j] + off[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < SPW; ++u) {
+        if (sw0 + u >= total) break;                     // warp-uniform
+        float ss = 0.0f;
+        if (live[u]) {
+            float acc[8];
+            fold_loaded<GDT, NT>(raw[u], acc);
+            average8<GDT, NT>(acc, avg);
+            if (SUMSQ) ss = sumsq8(acc);
+            const typename G::Raw out = G::pack(acc);
+            if (ALL) {
+#pragma unroll
+                for (int j = 0; j < NT; ++j) G::store_raw(const_cast<char*>(src[u][j]) + off[u], out);
+            } else {
+                G::store_raw(grads + ps[u].c * slab + off[u], out);
+            }
+        }
+        if (SUMSQ) {
+            const float t = warp_sum_f32(ss);
+            if (lane == 0) partials[ps[u].c * segs + ps[u].seg] = (double)t;
+        }
+    }
+}
+
 template <int GDT, int NT, bool ALL, bool SUMSQ>
 __global__ void __launch_bounds__(kBlock, ReduceBlocksPerSm<GDT, NT, ALL>::value)
 k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
@@ -71,6 +148,11 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
     const int64_t segs = segments_per_chunk(C);
     const int lane = threadIdx.x & 31;
     if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
+    if constexpr (ReduceSegsPerWarp<GDT, NT, ALL>::value > 1) {
+        reduce_segments<GDT, NT, ALL, SUMSQ, ReduceSegsPerWarp<GDT, NT, ALL>::value>(
+            grads, slab, C, groups, segs, avg, partials, lane);
+        return;
+    }
     const int64_t sw = global_warp();
     if (sw >= (int64_t)N * segs) return;                 // whole warps
     const SegPos p = seg_pos(sw, segs);
@@ -263,7 +345,8 @@ k_allgather(char* __restrict__ w, int64_t P, int64_t C, int N)
 template <int GDT, int NT, bool ALL, bool SUMSQ>
 static cudaError_t reduce_t(const Arena& a, const Avg& avg, void* grads, void* ws, cudaStream_t s)
 {
-    const unsigned blocks = blocks_for_segments(int64_t(a.N) * segments_per_chunk(a.C), 1);
+    const unsigned blocks = blocks_for_segments(int64_t(a.N) * segments_per_chunk(a.C),
+                                                ReduceSegsPerWarp<GDT, NT, ALL>::value);
     set_last_kernel_name(ALL ? "dpz_allreduce_avg" : SUMSQ ? "dpz_rs_avg_sumsq" : "dpz_rs_avg");
     k_reduce<GDT, NT, ALL, SUMSQ><<<blocks, kBlock, 0, s>>>(
         static_cast<char*>(grads), a.P, a.C, a.N, avg, static_cast<WsHeader*>(ws),
