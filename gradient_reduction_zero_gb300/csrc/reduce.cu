@@ -54,12 +54,6 @@ struct RangeBlocksPerSm {
                                  : GDT == 2 && NT == 8 ? 5 : 6;
 };
 
-// Ring-order reduce + average of every chunk, one segment per warp.
-// ALL = false: chunk c goes to slab c only (reduce-scatter).  ALL = true: to
-// every slab (all-reduce).  SUMSQ: per-segment sums of squares of the
-// averages.  NT > 0: N == NT known at compile time; NT == 0: any N, read from
-// n_rt.  With bf16 storage the reduce-scatter variants are held to 32
-// registers (ReduceBlocksPerSm).
 // Segments per warp of the reduce kernel.  A bf16 lane loads 16 bytes per
 // slab, so at N <= 2 one segment per warp keeps too few bytes in flight:
 // each warp then takes two consecutive segments of the list and issues all
@@ -135,6 +129,12 @@ __device__ __forceinline__ void reduce_segments(char* __restrict__ grads, int64_
     }
 }
 
+// Ring-order reduce + average of every chunk, one segment per warp (two for
+// bf16 at N <= 2, ReduceSegsPerWarp).  ALL = false: chunk c goes to slab c
+// only (reduce-scatter).  ALL = true: to every slab (all-reduce).  SUMSQ:
+// per-segment sums of squares of the averages.  NT > 0: N == NT known at
+// compile time; NT == 0: any N, read from n_rt.  Registers per thread follow
+// ReduceBlocksPerSm.
 template <int GDT, int NT, bool ALL, bool SUMSQ>
 __global__ void __launch_bounds__(kBlock, ReduceBlocksPerSm<GDT, NT, ALL>::value)
 k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
