@@ -9,9 +9,11 @@
 //   waits until those stores have read shared memory.  The arithmetic is
 //   adamw_elem, so the results are bit-identical to k_adamw.
 // - The whole step without clip (ring fold of the N slabs, average, AdamW,
-//   cast, N weight stores, optional averages store and norm partials), for
-//   compile-time N: one 1024-element tile of every slab plus master/m/v per
-//   128-thread CTA, the same load / update / store shape.
+//   cast, N weight stores, optional averages store and norm partials): one
+//   1024-element tile of every slab plus master/m/v per 128-thread CTA, the
+//   same load / update / store shape.  N up to 8 is compiled in; larger N
+//   fold at run time, where enough of their tiles stay resident per SM
+//   (zero1_fused_staged).
 // - Sums of squares of the owner chunks (the standalone norm): one 32 KB tile
 //   per 256-thread CTA, one bulk load, then each warp takes segments of the
 //   tile.  Large tiles keep ~220 KB of loads in flight per SM, which a
