@@ -157,12 +157,16 @@ k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __r
 
 // ------------------------------------------------------------ fold step
 
-// Shared memory of one fold tile: the tiles of the nr slabs (slab r's at
-// r * fold_slab_tile(GDT)), then master, m and v (fp32), then the cast weights.
-__host__ __device__ constexpr size_t fold_slab_tile(int GDT) { return (size_t)kTmaTile * (GDT == 0 ? 4 : 2); }
-constexpr size_t fold_tile_bytes(int GDT, int WDT, int nr)
+// Shared memory of one fold tile of `tile` elements: the tiles of the nr
+// slabs (slab r's at r * fold_slab_tile(GDT, tile)), then master, m and v
+// (fp32), then the cast weights.
+__host__ __device__ constexpr size_t fold_slab_tile(int GDT, int tile)
 {
-    return (size_t)nr * fold_slab_tile(GDT) + (size_t)kTmaTile * (12 + (WDT == 0 ? 4 : 2));
+    return (size_t)tile * (GDT == 0 ? 4 : 2);
+}
+constexpr size_t fold_tile_bytes(int GDT, int WDT, int nr, int tile)
+{
+    return (size_t)nr * fold_slab_tile(GDT, tile) + (size_t)tile * (12 + (WDT == 0 ? 4 : 2));
 }
 
 // Largest fold tile the run-time-N kernel takes: two CTAs still fit an SM's
@@ -175,9 +179,10 @@ constexpr size_t kFoldTileMaxBytes = 110 * 1024;
 // one at a time; both the same arithmetic as k_adamw), averages, adds its sum
 // of squares to its warp's segment partial (a warp covers one 256-element
 // segment of the tile), runs AdamW and casts.  With store_avg the averages
-// replace slab c's tile and are stored into slab c.
-template <int GDT, int WDT, int NT, bool SUMSQ>
-__global__ void __launch_bounds__(kTmaThreads)
+// replace slab c's tile and are stored into slab c.  TILE elements per CTA
+// (1024 or 512), 8 per thread.
+template <int GDT, int WDT, int NT, bool SUMSQ, int TILE>
+__global__ void __launch_bounds__(TILE / kGroup)
 k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
                   float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C,
                   int n_rt, Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
@@ -187,7 +192,7 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
     using WS = Group<WDT>;
     constexpr int GES = GS::kBytes;
     constexpr int WES = WS::kBytes;
-    constexpr size_t kSlabTile = fold_slab_tile(GDT);
+    constexpr size_t kSlabTile = fold_slab_tile(GDT, TILE);
     extern __shared__ __align__(128) unsigned char dsmem[];
     __shared__ __align__(8) uint64_t full;
     __shared__ int timed_out;
@@ -195,16 +200,16 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
     const int nr = NT > 0 ? NT : n_rt;
     unsigned char* const tg = dsmem;
     float* const tth = reinterpret_cast<float*>(dsmem + (size_t)nr * kSlabTile);
-    float* const tm = tth + kTmaTile;
-    float* const tv = tm + kTmaTile;
-    unsigned char* const tw = reinterpret_cast<unsigned char*>(tv + kTmaTile);
+    float* const tm = tth + TILE;
+    float* const tv = tm + TILE;
+    unsigned char* const tw = reinterpret_cast<unsigned char*>(tv + TILE);
 
-    const int64_t tiles_per_chunk = (C + kTmaTile - 1) / kTmaTile;
+    const int64_t tiles_per_chunk = (C + TILE - 1) / TILE;
     const int c = (int)(blockIdx.x / tiles_per_chunk);
     const int64_t tc = blockIdx.x - (int64_t)c * tiles_per_chunk;
-    const int64_t e = (int64_t)c * C + tc * kTmaTile;
-    const int64_t left = C - tc * kTmaTile;
-    const int n = (int)(left < kTmaTile ? left : kTmaTile);   // a multiple of 8
+    const int64_t e = (int64_t)c * C + tc * TILE;
+    const int64_t left = C - tc * TILE;
+    const int n = (int)(left < TILE ? left : TILE);   // a multiple of 8
     const int tid = threadIdx.x, lane = tid & 31;
     const int64_t gslab = P * GES;
 
@@ -275,7 +280,7 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
         const float tsum = warp_sum_f32(ss);                // whole warps
         const int seg = tid >> 5;
         if (lane == 0 && seg * kSegment < n)
-            partials[c * segments_per_chunk(C) + tc * (kTmaTile / kSegment) + seg] = (double)tsum;
+            partials[c * segments_per_chunk(C) + tc * (TILE / kSegment) + seg] = (double)tsum;
     }
     // the threads' shared-memory writes become visible to the bulk stores
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -423,20 +428,60 @@ cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void
     return tma_n<0, 0>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
 }
 
-template <int GDT, int WDT, int NT, bool SUMSQ>
+// Shared memory of an SM (sm_103a), and what each resident CTA costs beyond
+// its tile: the runtime's 1 KB reservation and the kernel's static barrier.
+constexpr size_t kSmemPerSm = 228 * 1024;
+constexpr size_t kCtaSmemOverhead = 1024 + 16;
+
+// Staged tiles resident on one SM when the grid fills it.
+static size_t fold_bytes_resident(size_t tile)
+{
+    return kSmemPerSm / (tile + kCtaSmemOverhead) * tile;
+}
+
+// The staged kernel keeps a stream going only with enough bytes in flight per
+// SM.  Measured on the 1.5B-class arenas without clip: tiles resident at 184
+// KB per SM and more ran at 7.08-7.18 TB/s, ahead of the fold kernel by 3-22
+// %; at 156 KB (two 78 KB tiles, e.g. N = 32 bf16 or N = 16 fp32) the fold
+// kernel was as fast or faster.  So for N > 8 the staged kernel is taken when
+// the resident tiles reach 176 KB.
+constexpr size_t kFoldMinResident = 176 * 1024;
+
+// Elements per CTA of the staged step for this arena: 1024 for N <= 8, and
+// for larger N the larger of 1024 and 512 whose tiles fit and stay resident
+// at kFoldMinResident; 0 when neither does (the fold kernel then runs).
+static int zero1_fused_tile(const Arena& a)
+{
+    if (a.N < 1) return 0;
+    if (a.N <= 8) return kTmaTile;
+    const int gdt = a.gdt == 0 ? 0 : 1;
+    for (int tile = kTmaTile; tile >= kTmaTile / 2; tile /= 2) {
+        const size_t bytes = fold_tile_bytes(gdt, a.wdt, a.N, tile);
+        if (bytes <= kFoldTileMaxBytes && fold_bytes_resident(bytes) >= kFoldMinResident)
+            return tile;
+    }
+    return 0;
+}
+
+bool zero1_fused_staged(const Arena& a)
+{
+    return zero1_fused_tile(a) != 0;
+}
+
+template <int GDT, int WDT, int NT, bool SUMSQ, int TILE = kTmaTile>
 static cudaError_t fused_tma_t(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
                                void* grads, float* master, float* m, float* v, void* weights,
                                void* ws, cudaStream_t s)
 {
-    auto fn = k_zero1_fused_tma<GDT, WDT, NT, SUMSQ>;
-    const size_t smem = fold_tile_bytes(GDT, WDT, NT > 0 ? NT : a.N);
+    auto fn = k_zero1_fused_tma<GDT, WDT, NT, SUMSQ, TILE>;
+    const size_t smem = fold_tile_bytes(GDT, WDT, NT > 0 ? NT : a.N, TILE);
     // the run-time-N kernel may take any tile up to kFoldTileMaxBytes
     const cudaError_t e = allow_smem(reinterpret_cast<const void*>(fn),
                                      NT > 0 ? smem : kFoldTileMaxBytes);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = (a.C + kTmaTile - 1) / kTmaTile * a.N;
+    const int64_t tiles = (a.C + TILE - 1) / TILE * a.N;
     set_last_kernel_name(SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused");
-    fn<<<(unsigned)tiles, kTmaThreads, smem, s>>>(
+    fn<<<(unsigned)tiles, TILE / kGroup, smem, s>>>(
         static_cast<char*>(grads), master, m, v, static_cast<char*>(weights), a.P, a.C, a.N, avg,
         h, store_avg ? 1 : 0, static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr);
     return cudaGetLastError();
@@ -473,8 +518,11 @@ static cudaError_t fused_tma_n(const Arena& a, const Avg& avg, const AdamArgs& h
         return fused_tma_t<GDT, WDT, 8, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
                                                 weights, ws, s);
     default:
-        return fused_tma_t<GDT, WDT, 0, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
-                                                weights, ws, s);
+        if (zero1_fused_tile(a) == kTmaTile)
+            return fused_tma_t<GDT, WDT, 0, SUMSQ>(a, avg, h, store_avg, grads, master, m, v,
+                                                    weights, ws, s);
+        return fused_tma_t<GDT, WDT, 0, SUMSQ, kTmaTile / 2>(a, avg, h, store_avg, grads, master,
+                                                              m, v, weights, ws, s);
     }
 }
 
@@ -488,33 +536,6 @@ static cudaError_t fused_tma_dt(const Arena& a, const Avg& avg, const AdamArgs& 
                                            ws, s);
     return fused_tma_n<GDT, WDT, false>(a, avg, h, store_avg, grads, master, m, v, weights, ws,
                                         s);
-}
-
-// Shared memory of an SM (sm_103a), and what each resident CTA costs beyond
-// its tile: the runtime's 1 KB reservation and the kernel's static barrier.
-constexpr size_t kSmemPerSm = 228 * 1024;
-constexpr size_t kCtaSmemOverhead = 1024 + 16;
-
-// Staged tiles resident on one SM when the grid fills it.
-static size_t fold_bytes_resident(size_t tile)
-{
-    return kSmemPerSm / (tile + kCtaSmemOverhead) * tile;
-}
-
-// The staged kernel keeps a stream going only with enough bytes in flight per
-// SM.  Measured on the 1.5B-class arenas without clip: tiles resident at 184
-// KB per SM and more ran at 7.08-7.18 TB/s, ahead of the fold kernel by 3-22
-// %; at 156 KB (two 78 KB tiles, e.g. N = 32 bf16 or N = 16 fp32) the fold
-// kernel was as fast or faster.  So for N > 8 the staged kernel is taken when
-// the resident tiles reach 176 KB.
-constexpr size_t kFoldMinResident = 176 * 1024;
-
-bool zero1_fused_staged(const Arena& a)
-{
-    if (a.N < 1) return false;
-    if (a.N <= 8) return true;
-    const size_t tile = fold_tile_bytes(a.gdt == 0 ? 0 : 1, a.wdt, a.N);
-    return tile <= kFoldTileMaxBytes && fold_bytes_resident(tile) >= kFoldMinResident;
 }
 
 cudaError_t launch_zero1_fused_tma(const Arena& a, const Avg& avg, const AdamArgs& h,
