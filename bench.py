@@ -589,6 +589,12 @@ def segment_bounds(P: int, N: int, k: int):
     return [(edges[i], edges[i + 1] - edges[i]) for i in range(len(edges) - 1)][::-1]
 
 
+# The GEMM stand-in for a backward: bf16 matmuls of GEMM_DIM^3 (1.1 TFLOP each)
+# per bucket.
+GEMM_DIM = 8192
+GEMM_PER_BUCKET = 3
+
+
 def run_buckets(args, w, G, T, M, V, W, ws, nrm, cfg, stream, rs_ms):
     """Overlap of the reduce-scatter with a simulated backward pass.  The
     backward writes the gradient arena bucket by bucket (the seeded input
@@ -597,7 +603,10 @@ def run_buckets(args, w, G, T, M, V, W, ws, nrm, cfg, stream, rs_ms):
     a second stream waits on it and reduces that bucket
     (dp_reduce_scatter_avg_range, capped at one block per SM so that the
     backward keeps most of the GPU), then finalises the norm and runs
-    dp_zero1_update once the last bucket is in.  Both compute the same step."""
+    dp_zero1_update once the last bucket is in.  Both compute the same step.
+    With --backward gemm each bucket's backward is instead GEMM_PER_BUCKET
+    bf16 matmuls (the tensor cores, as a real backward's) followed by a copy
+    of the bucket's gradients from a pre-generated arena."""
     import torch
     import gradient_reduction_zero_gb300.dpz as dpz
     es = w.grad_bytes()
@@ -609,10 +618,24 @@ def run_buckets(args, w, G, T, M, V, W, ws, nrm, cfg, stream, rs_ms):
     comm = torch.cuda.Stream(priority=-1)
     max_ctas = torch.cuda.get_device_properties(G.device).multi_processor_count
 
-    def backward_bucket(lo, n):
-        for r in range(w.N):
-            I.dev_fill(base + (r * w.P + lo) * es, w.gdtype, lo, n, w.grad_seed + r,
-                       I.STREAM_GRAD, w.grad, main.cuda_stream)
+    if args.backward == "gemm":
+        src = G.clone()                                  # the gradients the backward "produces"
+        gen = torch.Generator(device=G.device).manual_seed(7)
+        A = torch.randn(GEMM_DIM, GEMM_DIM, device=G.device, generator=gen).to(torch.bfloat16)
+        B = torch.randn(GEMM_DIM, GEMM_DIM, device=G.device, generator=gen).to(torch.bfloat16)
+        Cm = torch.empty(GEMM_DIM, GEMM_DIM, device=G.device, dtype=torch.bfloat16)
+        Gv, Sv = G.view(w.N, w.P), src.view(w.N, w.P)
+
+        def backward_bucket(lo, n):
+            with torch.cuda.stream(main):
+                for _ in range(GEMM_PER_BUCKET):
+                    torch.matmul(A, B, out=Cm)
+                Gv[:, lo:lo + n].copy_(Sv[:, lo:lo + n])
+    else:
+        def backward_bucket(lo, n):
+            for r in range(w.N):
+                I.dev_fill(base + (r * w.P + lo) * es, w.gdtype, lo, n, w.grad_seed + r,
+                           I.STREAM_GRAD, w.grad, main.cuda_stream)
 
     def serial():
         for lo, n in buckets:
@@ -652,7 +675,8 @@ def run_buckets(args, w, G, T, M, V, W, ws, nrm, cfg, stream, rs_ms):
     t_over = timed(overlapped)
     # only the reduce-scatter can run before the last bucket exists; the norm
     # and the update need every bucket
-    return {"buckets": len(buckets), "max_ctas": max_ctas, "backward_ms": round(t_back, 3),
+    return {"buckets": len(buckets), "backward": args.backward, "max_ctas": max_ctas,
+            "backward_ms": round(t_back, 3),
             "serial_ms": round(t_serial, 3), "overlapped_ms": round(t_over, 3),
             "reduce_scatter_ms": round(rs_ms, 3),
             "reduce_scatter_hidden_fraction": round((t_serial - t_over) / rs_ms, 3)}
@@ -831,6 +855,10 @@ def main(argv=None):
                     help="override the workload's clip norm (0: no clipping, one fused kernel)")
     ap.add_argument("--buckets", type=int, default=0,
                     help="also measure a bucketed step overlapped with a simulated backward")
+    ap.add_argument("--backward", choices=("fill", "gemm"), default="fill",
+                    help="the simulated backward of --buckets: the seeded generator writing each "
+                         "bucket (bound by instruction issue), or bf16 GEMMs on the tensor cores "
+                         "followed by a copy of the bucket's gradients")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured in a CUDA graph and replayed")
     ap.add_argument("--acc32", action="store_true",
