@@ -159,7 +159,9 @@ def test_range_without_partials_any_alignment():
         assert same_bits(out[c, sl], a[c, sl])
 
 
-@pytest.mark.parametrize("N,C,gdt,acc32", [(7, 1032, "bf16", False), (7, 1032, "bf16", True),
+@pytest.mark.parametrize("N,C,gdt,acc32", [(1, 4104, "bf16", False), (1, 4104, "bf16", True),
+                                           (2, 2056, "bf16", False), (2, 2056, "bf16", True),
+                                           (7, 1032, "bf16", False), (7, 1032, "bf16", True),
                                            (8, 776, "bf16", True), (12, 520, "bf16", False),
                                            (5, 2000, "f32", False), (8, 776, "f32", False),
                                            (12, 520, "f32", False), (16, 264, "f32", False)])
@@ -167,7 +169,9 @@ def test_range_partials_match_whole_arena(N, C, gdt, acc32):
     """Every register bound of the range kernel (compile-time N up to 8, the
     run-time fold beyond, both storage dtypes, fp32 accumulation): the ranges'
     averages are the oracle's, bit for bit, and the norm from their partials
-    equals the norm of the whole-arena reduce."""
+    equals the norm of the whole-arena reduce.  At N = 1 and 2 with bf16
+    storage the whole-arena reduce takes two segments per warp; 17 and 18
+    segments leave the last warp half idle and make warps straddle chunks."""
     w = I.TINY.with_(N=N, P=N * C, gdtype=gdt, grad=I.Dist(I.NORMAL, 1e-3), grad_seed=N + C)
     g = I.arena_host(w)
     P = w.P
