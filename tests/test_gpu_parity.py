@@ -288,6 +288,22 @@ def test_random_shapes(N, C, gdt, wdt, clip, acc32, seed):
     assert a[5] == b[5]
 
 
+@pytest.mark.parametrize("N,C", [(12, 520), (32, 264), (64, 72)])
+@pytest.mark.parametrize("clip", [0.0, 1e-3])
+def test_large_n_fp32_accumulating_step(N, C, clip):
+    """The fp32-accumulating bf16 ring at large N, where the step without clip
+    runs the staged kernel with a run-time fold on 1024- (N = 12) or
+    512-element tiles (N = 32, 64): against the oracle, and against the four
+    separate calls bit for bit."""
+    w, g, th, m, v, wts = make_problem(N, C, "bf16", "bf16", clip, seed=N + 7)
+    a = run_gpu_step(w, g, th, m, v, wts, fused=True, acc32=True)
+    check_step(w, g, th, m, v, wts, a, acc32=True)
+    b = run_gpu_step(w, g, th, m, v, wts, fused=False, acc32=True)
+    for x, y in zip(a[:5], b[:5]):
+        assert same_bits(x, y)
+    assert a[5] == b[5]
+
+
 def test_deterministic():
     w, g, th, m, v, wts = make_problem(8, 12344, "bf16", "bf16", 1e-3, seed=1)
     a = run_gpu_step(w, g, th, m, v, wts)
