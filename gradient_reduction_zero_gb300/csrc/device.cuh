@@ -234,9 +234,10 @@ __device__ __forceinline__ void fold_loaded(const typename Group<GDT>::Raw raw[N
 //   acc = x[c+1];  acc = R(acc + x[c+j]) for j = 2..N   (ranks mod N).
 // slab: bytes per slab; off: byte offset of the group inside a slab.  One
 // slab at a time: few registers, so many warps stay resident and keep loads
-// in flight (a version batching eight loads per thread held 76 registers and
-// ran the N = 3 reduce at 28 % of the copy peak; this form and more warps
-// reach about 80 %, and the compile-time folds for N <= 8 about 97-109 %).
+// in flight.  A version batching eight loads per thread held 76 registers
+// and ran the N = 3 reduce at 28 % of the copy peak; this form, used for
+// N > 8 (the compile-time folds take N <= 8), reduces at 102-109 % of it for
+// N = 12 to 32.
 template <int GDT>
 __device__ __forceinline__ void ring_fold(const char* __restrict__ grads, int64_t slab,
                                           int64_t off, int c, int N, float acc[8])
