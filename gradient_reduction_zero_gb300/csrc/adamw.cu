@@ -192,7 +192,8 @@ static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bo
     return cudaGetLastError();
 }
 
-// The fold kernel for the N that the staged kernel does not take (N > 8).
+// The fold kernel for the arenas the staged kernel does not take (large N
+// whose slab tiles cannot stay resident, zero1_fused_staged).
 template <int GDT, int WDT, bool SUMSQ>
 static cudaError_t fused_n(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
                            void* grads, float* master, float* m, float* v, void* weights,
