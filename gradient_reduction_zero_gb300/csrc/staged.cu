@@ -12,8 +12,8 @@
 //   cast, N weight stores, optional averages store and norm partials): one
 //   1024-element tile of every slab plus master/m/v per 128-thread CTA, the
 //   same load / update / store shape.  N up to 8 is compiled in; larger N
-//   fold at run time, where enough of their tiles stay resident per SM
-//   (zero1_fused_staged).
+//   fold at run time, on 1024- or 512-element tiles (64 threads), where
+//   enough of their tiles stay resident per SM (zero1_fused_tile).
 // - Sums of squares of the owner chunks (the standalone norm): one 32 KB tile
 //   per 256-thread CTA, one bulk load, then each warp takes segments of the
 //   tile.  Large tiles keep ~220 KB of loads in flight per SM, which a
@@ -170,8 +170,8 @@ constexpr size_t fold_tile_bytes(int GDT, int WDT, int nr, int tile)
 }
 
 // Largest fold tile the run-time-N kernel takes: two CTAs still fit an SM's
-// 228 KB (bf16 gradients up to N = 47, fp32 up to N = 23; one more with
-// bf16 weights).
+// 228 KB (1024-element tiles: bf16 gradients up to N = 47, fp32 up to
+// N = 23; 512-element tiles: fp32 up to N = 51; one more with bf16 weights).
 constexpr size_t kFoldTileMaxBytes = 110 * 1024;
 
 // The step without clip: every lane folds its 8 elements over the slab tiles
