@@ -16,9 +16,8 @@
 //   enough of their tiles stay resident per SM (zero1_fused_tile).
 // - Sums of squares of the owner chunks (the standalone norm): one 32 KB tile
 //   per 256-thread CTA, one bulk load, then each warp takes segments of the
-//   tile.  Large tiles keep ~220 KB of loads in flight per SM, which a
-//   read-only stream needs to cover the DRAM latency under load; 16-byte
-//   loads from registers reached 74 % of the copy peak, this 100 %.
+//   tile.  Large tiles keep ~220 KB of loads in flight per SM; with 64 KB this
+//   kernel ran at 67 % of the copy peak, with 224 KB at 100 %.
 //
 // Every wait on an mbarrier is bounded by the SM clock: if a tile has not
 // arrived after about two seconds the CTA sets the device error flag that
