@@ -17,6 +17,13 @@ PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
 # (name, text in oracle.c, replacement)
 MUTANTS = [
     ("average divides by N+1", "a[i] = a[i] / (float)N;", "a[i] = a[i] / (float)(N + 1);"),
+    ("fp32 average multiplies by RN(1/N)", "a[i] = a[i] / (float)N;",
+     "a[i] = a[i] * (1.0f / (float)N);"),
+    # (the same mistake in the per-hop bf16 branch is not one: for every bf16
+    # sum and every N up to 64 both quotients round to the same bf16)
+    ("fp32-accumulating average multiplies by RN(1/N)",
+     "a[i] = orc_bf16_to_f32(orc_f32_to_bf16(a[i] / (float)N));",
+     "a[i] = orc_bf16_to_f32(orc_f32_to_bf16(a[i] * (1.0f / (float)N)));"),
     ("sum instead of average", "a[i] = a[i] / (float)N;\n            } else if (R->dt == ORC_BF16_ACC32)",
      "a[i] = a[i];\n            } else if (R->dt == ORC_BF16_ACC32)"),
     ("bf16 rounds half up", "b += 0x7fffu + ((b >> 16) & 1u);", "b += 0x8000u;"),

@@ -637,6 +637,52 @@ def test_acc32_is_one_rounding_of_the_fp32_fold(N):
         assert np.array_equal(a[c, sl], want)
 
 
+def _bf16_bits(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("N", [3, 7])
+def test_acc32_average_is_the_ieee_quotient_near_bf16_ties(N):
+    """The average divides (Lab 09 — Parallelism, simulated, §2: sum, then
+    divide by N).  A product with RN(1/N) differs from the correctly rounded
+    quotient in the last fp32 bit for about a third of the sums, and that
+    reaches the bf16 result only where the quotient sits next to a bf16 tie:
+    about one sum in 10^5.  So the sums here are searched for exactly those
+    cases, each split into three exact bf16 parts placed on the first three
+    ranks of its chunk's ring order, so that the fp32 fold reproduces it."""
+    rng = np.random.default_rng(100 + N)
+    bits = rng.integers(0x3F800000, 0x40000000, 2_000_000, dtype=np.uint32)   # [1, 2)
+    s = bits.view(np.float32)
+    q_ieee = (s.astype(np.float64) / N).astype(np.float32)
+    q_recip = (s * (np.float32(1) / np.float32(N))).astype(np.float32)
+    hit = np.nonzero(_bf16_bits(q_ieee) != _bf16_bits(q_recip))[0][:4]
+    assert len(hit) >= 2
+    C = 8
+    x = np.zeros((N, N * C), dtype=np.float32)
+    sums = s[hit]
+    for e, a in enumerate(sums):
+        hi = (np.array([a]).view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)[0]
+        rem = np.float32(a - hi)
+        mid = (np.array([rem]).view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)[0]
+        lo = np.float32(rem - mid)
+        for part in (hi, mid, lo):
+            assert O.bf16_to_f32(O.f32_to_bf16(np.array([part], dtype=np.float32)))[0] == part
+        assert np.float32(np.float32(hi + mid) + lo) == a
+        # chunk 0 is folded in rank order 1, 2, ..., N - 1, 0
+        x[1, e], x[2, e], x[3 % N, e] = hi, mid, lo
+    xb = O.f32_to_bf16(x)
+    O.reduce_scatter_avg(xb, acc32=True)
+    for e, a in enumerate(sums):
+        exact = Fraction(float(a)) / N
+        q = np.float32(float(a) / N)                     # nearest float32 to a / N
+        ulp = np.spacing(q)
+        assert abs(Fraction(float(q)) - exact) < Fraction(float(ulp)) / 2
+        want = _bf16_bits(np.array([q]))[0]
+        assert int(xb[0, e]) == int(want)
+        assert int(want) != int(_bf16_bits(np.array([q_recip[hit[e]]]))[0])
+
+
 def test_acc32_differs_from_per_hop_rounding():
     """256 + 1 + 1 in a bf16 ring: per-hop rounding loses both ones (257
     rounds to 256), fp32 accumulation keeps them (258 / 3 = 86)."""
