@@ -164,9 +164,12 @@ def check_step(w, g, th, m, v, wts, out, check_avg=True, acc32=False):
 
 # N = 24 (fp32 gradients) and N = 48 (bf16) put the N slab tiles of the staged
 # step exactly at its shared-memory limit with bf16 weights and just past it
-# with fp32 weights, so both sides of that switch run.
+# with fp32 weights, so both sides of that switch run.  N = 32 with C = 1288
+# runs three 512-element tiles per chunk, the last one ragged, in every dtype
+# pair.
 STEP_SHAPES = [(1, 8), (1, 4104), (2, 2056), (3, 1000), (4, 1024), (4, 6152), (5, 2000),
-               (8, 12344), (16, 520), (24, 1032), (48, 264), (64, 72), (4, 3_000_016)]
+               (8, 12344), (16, 520), (24, 1032), (32, 1288), (48, 264), (64, 72),
+               (4, 3_000_016)]
 
 
 @pytest.mark.parametrize("N,C", STEP_SHAPES)
