@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdpz.so")
 
 SOURCES = ["api.cpp", "reduce.cu", "adamw.cu", "staged.cu", "norm_static.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("internal.h", "device.cuh")] + \
+HEADERS = [os.path.join(CSRC, h) for h in ("internal.h", "device.cuh", "bulk.cuh")] + \
     [os.path.join(INCLUDE, "dpz.h")]
 
 NVCC_FLAGS = [

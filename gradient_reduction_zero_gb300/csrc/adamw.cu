@@ -104,10 +104,15 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
     if (sw >= (int64_t)N * segs) return;                 // whole warps
     const SegPos p = seg_pos(sw, segs);
 
-    // clip scale from the global norm of the averaged gradient
+    // clip scale from the global norm of the averaged gradient; a norm whose
+    // input was not read in full is unknown, and then nothing is updated
     float scale = 1.0f;
     bool do_scale = false;
     if (!FOLD && h.clip > 0.0f) {
+        if (hdr->status & DPZ_STATUS_NORM_SKIPPED) {
+            if (threadIdx.x == 0) atomicOr(&hdr->status, DPZ_STATUS_UPDATE_SKIPPED);
+            return;
+        }
         const float nrm = hdr->norm;
         if (nrm > h.clip) {
             scale = __fdiv_rn(h.clip, nrm);
@@ -172,6 +177,7 @@ k_zero1_small(char* __restrict__ grads, float* __restrict__ master, float* __res
         hdr->sumsq = r;
         hdr->norm = nrm;
         hdr->nparts = (uint32_t)total;
+        hdr->status = 0u;          // plain loads: no tile is ever skipped here
         hdr->arrive = 0u;
         if (norm_out) *norm_out = nrm;
     }
@@ -207,7 +213,7 @@ template <int GDT, int WDT>
 static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                             bool bcast, bool store_avg, void* grads, float* master, float* m,
                             float* v, void* weights, void* ws, cudaStream_t s,
-                            int64_t avg_stride)
+                            int64_t avg_stride, float* norm_out, bool early)
 {
     if (src == AdamSrc::kFold) {
         if (zero1_fused_staged(a))   // staged through shared memory by bulk copies (staged.cu)
@@ -220,7 +226,8 @@ static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, A
                                         s);
     }
     if (bcast)      // staged through shared memory by bulk copies (staged.cu)
-        return launch_adamw_bcast_tma(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+        return launch_adamw_bcast_tma(a, h, grads, avg_stride, master, m, v, weights, ws,
+                                      norm_out, early, s);
     return adamw_t<GDT, WDT, 0, false, false, false>(a, avg, h, false, grads, master, m, v,
                                                     weights, ws, s, avg_stride);
 }
@@ -269,7 +276,8 @@ cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h
 
 cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                          bool bcast, bool store_avg, void* grads, float* master, float* m,
-                         float* v, void* weights, void* ws, cudaStream_t s, int64_t avg_stride)
+                         float* v, void* weights, void* ws, cudaStream_t s, int64_t avg_stride,
+                         float* norm_out, bool early)
 {
     if (a.gdt == 2) {
         // fp32-accumulating bf16 ring: only the fold differs; stored averages
@@ -277,26 +285,26 @@ cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, Adam
         if (src == AdamSrc::kFold) {
             if (a.wdt == 1)
                 return adamw_dt<2, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                                      weights, ws, s, avg_stride);
+                                      weights, ws, s, avg_stride, norm_out, early);
             return adamw_dt<2, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                                  weights, ws, s, avg_stride);
+                                  weights, ws, s, avg_stride, norm_out, early);
         }
         Arena b = a;
         b.gdt = 1;
         return launch_adamw(b, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws, s,
-                            avg_stride);
+                            avg_stride, norm_out, early);
     }
     if (a.gdt == 1 && a.wdt == 1)
         return adamw_dt<1, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                              weights, ws, s, avg_stride);
+                              weights, ws, s, avg_stride, norm_out, early);
     if (a.gdt == 1 && a.wdt == 0)
         return adamw_dt<1, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                              weights, ws, s, avg_stride);
+                              weights, ws, s, avg_stride, norm_out, early);
     if (a.gdt == 0 && a.wdt == 1)
         return adamw_dt<0, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                              weights, ws, s, avg_stride);
+                              weights, ws, s, avg_stride, norm_out, early);
     return adamw_dt<0, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                          weights, ws, s, avg_stride);
+                          weights, ws, s, avg_stride, norm_out, early);
 }
 
 }  // namespace dpz

@@ -10,6 +10,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -87,20 +88,35 @@ struct Range {
     uintptr_t lo, hi;
 };
 
-int check_disjoint(const std::vector<Range>& rs)
-{
-    for (size_t i = 0; i < rs.size(); ++i)
-        for (size_t j = i + 1; j < rs.size(); ++j)
-            if (rs[i].lo < rs[j].hi && rs[j].lo < rs[i].hi)
-                return fail(DPZ_ERR_INVALID_ARG, "buffers %s and %s overlap", rs[i].name,
-                            rs[j].name);
-    return DPZ_OK;
-}
-
 Range range(const char* name, const void* p, int64_t bytes)
 {
     uintptr_t lo = reinterpret_cast<uintptr_t>(p);
     return {name, lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+// The byte ranges of one call's buffers, held on the stack (no allocation on
+// the launch path).  A NULL buffer is not added.
+struct Ranges {
+    Range r[8];
+    int n = 0;
+    Ranges(std::initializer_list<Range> rs)
+    {
+        for (const Range& x : rs) r[n++] = x;
+    }
+    void add(const char* name, const void* p, int64_t bytes)
+    {
+        if (p != nullptr) r[n++] = range(name, p, bytes);
+    }
+};
+
+int check_disjoint(const Ranges& rs)
+{
+    for (int i = 0; i < rs.n; ++i)
+        for (int j = i + 1; j < rs.n; ++j)
+            if (rs.r[i].lo < rs.r[j].hi && rs.r[j].lo < rs.r[i].hi)
+                return fail(DPZ_ERR_INVALID_ARG, "buffers %s and %s overlap", rs.r[i].name,
+                            rs.r[j].name);
+    return DPZ_OK;
 }
 
 int check_cfg(const dpz_adamw_cfg* cfg)
@@ -153,7 +169,7 @@ AdamArgs make_adam(const dpz_adamw_cfg* cfg)
 
 struct Profiler {
     std::mutex mu;
-    bool on = false;
+    std::atomic<bool> on{false};     // read without the lock on every launch
     int cap = 0;
     int used = 0;
     std::vector<cudaEvent_t> ev;
@@ -165,9 +181,10 @@ template <class F>
 int launch(cudaStream_t s, F&& f)
 {
     int slot = -1;
-    {
+    if (g_prof.on.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lk(g_prof.mu);
-        if (g_prof.on && g_prof.used < g_prof.cap) slot = g_prof.used++;
+        if (g_prof.on.load(std::memory_order_relaxed) && g_prof.used < g_prof.cap)
+            slot = g_prof.used++;
     }
     if (slot >= 0) cudaEventRecord(g_prof.ev[2 * slot], s);
     cudaError_t e = f();
@@ -203,11 +220,21 @@ DPZ_API const char* dpz_version(void) { return "dpz 0.1 (sm_103a)"; }
 
 DPZ_API int64_t dpz_launch_count(void) { return g_launches.load(); }
 
-DPZ_API int dpz_selftest_staged_timeout(void* buf, void* stream)
+DPZ_API int dpz_selftest_staged_timeout(int kernel, void* buf, void* stream)
 {
-    DPZ_TRY(check_ptr(buf, "buf"));
+    if (kernel != DPZ_SELFTEST_UPDATE && kernel != DPZ_SELFTEST_NORM &&
+        kernel != DPZ_SELFTEST_STEP)
+        return fail(DPZ_ERR_INVALID_ARG, "unknown self-test kernel %d", kernel);
+    if (buf == nullptr) return fail(DPZ_ERR_INVALID_ARG, "buf is NULL");
+    if (reinterpret_cast<uintptr_t>(buf) % 256 != 0)
+        return fail(DPZ_ERR_ALIGN, "buf is not 256-byte aligned");
     cudaStream_t s = as_stream(stream);
-    DPZ_TRY(launch(s, [&] { return launch_staged_timeout_selftest(buf, s); }));
+    DPZ_TRY(launch(s, [&] { return launch_staged_timeout_selftest(kernel, buf, s); }));
+    if (kernel != DPZ_SELFTEST_UPDATE) {
+        // the finalisation turns the skipped tile's markers into the status
+        float* nrm = reinterpret_cast<float*>(static_cast<char*>(buf) + kSelftestNormOut);
+        DPZ_TRY(launch(s, [&] { return launch_norm_finalize(kSelftestArena, buf, nrm, s); }));
+    }
     return ok();
 }
 
@@ -267,9 +294,9 @@ DPZ_API int dp_grad_global_norm(const void* grads, int64_t P, int N, int gdtype,
     DPZ_TRY(check_dtype(gdtype, "gradient", true));
     DPZ_TRY(check_ptr(grads, "grads", gdtype));
     DPZ_TRY(check_ptr(ws, "ws"));
-    std::vector<Range> rs = {range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
-                             range("ws", ws, (int64_t)dpz_workspace_bytes(P, N))};
-    if (norm_out) rs.push_back(range("norm_out", norm_out, 4));
+    Ranges rs = {range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
+                 range("ws", ws, (int64_t)dpz_workspace_bytes(P, N))};
+    rs.add("norm_out", norm_out, 4);
     DPZ_TRY(check_disjoint(rs));
     const Arena a = make_arena(P, N, gdtype, gdtype);
     cudaStream_t s = as_stream(stream);
@@ -293,12 +320,11 @@ static int check_step_buffers(const void* grads, const float* master, const floa
     DPZ_TRY(check_ptr(v, "v", DPZ_F32));
     DPZ_TRY(check_ptr(weights, "weights", wdtype));
     if (need_ws) DPZ_TRY(check_ptr(ws, "ws"));
-    std::vector<Range> rs = {range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
-                             range("master", master, P * 4), range("m", m, P * 4),
-                             range("v", v, P * 4),
-                             range("weights", weights, int64_t(N) * P * elem_bytes(wdtype))};
-    if (ws) rs.push_back(range("ws", ws, (int64_t)dpz_workspace_bytes(P, N)));
-    if (norm_out) rs.push_back(range("norm_out", norm_out, 4));
+    Ranges rs = {range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
+                 range("master", master, P * 4), range("m", m, P * 4), range("v", v, P * 4),
+                 range("weights", weights, int64_t(N) * P * elem_bytes(wdtype))};
+    rs.add("ws", ws, (int64_t)dpz_workspace_bytes(P, N));
+    rs.add("norm_out", norm_out, 4);
     return check_disjoint(rs);
 }
 
@@ -348,9 +374,12 @@ DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v, void* 
         // cast + all-gather reading the stored averages
         DPZ_TRY(launch(s, [&] { return launch_reduce(a, avg, grads, false, ws, s); }));
         DPZ_TRY(launch(s, [&] { return launch_norm_finalize(a, ws, norm_out, s); }));
+        // launched early behind the finalisation: every kernel before it in
+        // the step was launched behind all earlier work on the stream, so its
+        // master/m/v loads may start before the finalisation ends
         DPZ_TRY(launch(s, [&] {
             return launch_adamw(a, avg, h, AdamSrc::kLoadOwner, true, false, grads, master, m, v,
-                                weights, ws, s, P);
+                                weights, ws, s, P, norm_out, true);
         }));
     } else if (norm_out && zero1_fits_one_block(a)) {
         // a small arena: the step and its norm in one single-block launch
@@ -428,12 +457,10 @@ DPZ_API int dp_reduce_scatter_avg_bucket(const void* staging, int64_t lo, int64_
     DPZ_TRY(check_ptr(shards, "shards", gdtype));
     DPZ_TRY(check_range(P, N, lo, n, ws != nullptr));
     const int es = elem_bytes(gdtype);
-    std::vector<Range> rs = {range("staging", staging, int64_t(N) * n * es),
-                             range("shards", shards, P * es)};
-    if (ws) {
-        DPZ_TRY(check_ptr(ws, "ws"));
-        rs.push_back(range("ws", ws, (int64_t)dpz_workspace_bytes(P, N)));
-    }
+    Ranges rs = {range("staging", staging, int64_t(N) * n * es),
+                 range("shards", shards, P * es)};
+    if (ws) DPZ_TRY(check_ptr(ws, "ws"));
+    rs.add("ws", ws, (int64_t)dpz_workspace_bytes(P, N));
     DPZ_TRY(check_disjoint(rs));
     const Arena a = make_arena(P, N, gdtype, gdtype);
     const Avg avg = make_avg(N);
@@ -472,11 +499,10 @@ static int update_common(const void* avg_src, int64_t avg_stride, int64_t avg_el
     DPZ_TRY(check_ptr(weights, "weights", wdtype));
     const bool clip = cfg->clip_norm > 0.0f;
     if (clip) DPZ_TRY(check_ptr(ws, "ws"));
-    std::vector<Range> rs = {range(what, avg_src, avg_elems * elem_bytes(gdtype)),
-                             range("master", master, P * 4), range("m", m, P * 4),
-                             range("v", v, P * 4),
-                             range("weights", weights, int64_t(N) * P * elem_bytes(wdtype))};
-    if (ws) rs.push_back(range("ws", ws, (int64_t)dpz_workspace_bytes(P, N)));
+    Ranges rs = {range(what, avg_src, avg_elems * elem_bytes(gdtype)),
+                 range("master", master, P * 4), range("m", m, P * 4), range("v", v, P * 4),
+                 range("weights", weights, int64_t(N) * P * elem_bytes(wdtype))};
+    rs.add("ws", ws, (int64_t)dpz_workspace_bytes(P, N));
     DPZ_TRY(check_disjoint(rs));
     const Arena a = make_arena(P, N, gdtype, wdtype);
     const Avg avg = make_avg(N);
@@ -521,12 +547,12 @@ DPZ_API int dp_grad_global_norm_static(const void* grads, int64_t P, int N, int 
                     N, (long long)P, need, static_scratch_bytes());
     DPZ_TRY(check_disjoint({range("grads", grads, int64_t(N) * P * elem_bytes(gdtype)),
                             range("norm_out", norm_out, 4)}));
+    cudaStream_t s = as_stream(stream);
     void* ws = nullptr;
-    const cudaError_t e = static_scratch_address(&ws);
+    const cudaError_t e = static_scratch_address(&ws, s);
     if (e != cudaSuccess)
         return fail(DPZ_ERR_CUDA, "address of the static norm scratch: %s", cudaGetErrorString(e));
     const Arena a = make_arena(P, N, gdtype, gdtype);
-    cudaStream_t s = as_stream(stream);
     DPZ_TRY(launch(s, [&] { return launch_norm_owned(a, grads, ws, s); }));
     DPZ_TRY(launch(s, [&] { return launch_norm_finalize(a, ws, norm_out, s); }));
     return ok();

@@ -11,6 +11,16 @@ namespace dpz {
 // About two seconds of SM clock: the bound on every wait for a bulk copy.
 constexpr long long kWaitLimitCycles = 4000000000LL;
 
+// How a staged kernel waits for its tile: the bound on each wait (SM clock
+// cycles), and the bytes its barrier expects beyond the tile's loads.  That is
+// 0 except in the self-test of the timeout path, where the barrier then never
+// completes and the wait runs out (with a short bound, so the test is quick).
+struct WaitSpec {
+    long long limit;
+    uint32_t extra_tx;
+};
+constexpr WaitSpec kWaitNormal{kWaitLimitCycles, 0u};
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p)
 {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -43,15 +53,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for phase 0 of the barrier, at most kWaitLimitCycles; false if the
-// wait ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar)
+// Wait for the phase of the barrier with the given parity, at most `limit`
+// SM clock cycles; false if the wait ran out.  The clock keeps counting while
+// the context is switched out, so a wait that sees the limit pass polls once
+// more before it gives up: a copy that completed while the context was off the
+// GPU is then still taken.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, long long limit,
+                                                  uint32_t parity = 0)
 {
-    if (mbar_try_wait(bar, 0)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, 0))
-        if (clock64() - t0 > kWaitLimitCycles) return false;
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > limit) return mbar_try_wait(bar, parity);
     return true;
+}
+
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream, if it was launched with programmatic stream serialisation,
+// begin before this one has finished; that kernel's wait_prior then blocks
+// until every earlier kernel has completed and its writes are visible.  In a
+// kernel launched the ordinary way, wait_prior returns at once.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_prior()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // global -> shared, completing `bytes` on the mbarrier

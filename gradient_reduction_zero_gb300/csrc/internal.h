@@ -6,6 +6,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "dpz.h"
+
 #if defined(__CUDACC__)
 #define DPZ_HD __host__ __device__
 #else
@@ -28,7 +30,19 @@ struct WsHeader {
     float norm;        // sqrt(sumsq) rounded to float
     uint32_t nparts;   // segment partials the last norm used
     uint32_t arrive;   // finalisation blocks done (reset by every producer)
+    uint32_t status;   // DPZ_STATUS_* bits: written whole by every norm
+                       // finalisation, bit DPZ_STATUS_UPDATE_SKIPPED set by the
+                       // update kernels that follow it
 };
+static_assert(offsetof(WsHeader, status) == DPZ_WS_STATUS_OFFSET,
+              "the status word sits where dpz.h says");
+
+// A segment partial is a sum of squares: +0 or more, +inf or NaN, never
+// negative.  A staged kernel that gives up on a tile writes one of these
+// negative markers into the tile's partial slots instead, and the
+// finalisation turns them into a NaN norm and status bits.
+constexpr double kPartialNormSkipped = -1.0;   // the tile was not read
+constexpr double kPartialStepSkipped = -2.0;   // nor was its update written
 
 DPZ_HD inline int64_t segments_per_chunk(int64_t C) { return (C + kSegment - 1) / kSegment; }
 
@@ -95,11 +109,21 @@ struct RangeArgs {
 };
 cudaError_t launch_reduce_range(const Arena& a, const Avg& avg, const RangeArgs& g, void* ws,
                                 cudaStream_t s);
+// The finalisation is launched with programmatic stream serialisation: it
+// may start while the kernel before it drains, and waits for that kernel's
+// writes before it reads any partial.
 cudaError_t launch_norm_finalize(const Arena& a, void* ws, float* norm_out, cudaStream_t s);
+// norm_out: where the step's norm went (the bulk-copy staged update writes
+// NaN there if it gives up on a tile; may be NULL).  early: the staged update
+// may begin while the previous kernel on the stream finishes, issuing its
+// master/m/v loads before it waits for that kernel (programmatic dependent
+// launch).  Only for a kernel whose earlier work on the stream was launched
+// the ordinary way behind everything that writes master/m/v, as in
+// dp_zero1_step.
 cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                          bool bcast, bool store_avg, void* grads, float* master, float* m,
                          float* v, void* weights, void* ws, cudaStream_t s,
-                         int64_t avg_stride);
+                         int64_t avg_stride, float* norm_out = nullptr, bool early = false);
 cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 
 // The whole step without clip, norm included, in one single-block launch, for
@@ -118,7 +142,8 @@ cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h
 // read_and_clear_pipeline_error returns.
 cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
                                    int64_t avg_stride, float* master, float* m, float* v,
-                                   void* weights, const void* ws, cudaStream_t s);
+                                   void* weights, void* ws, float* norm_out, bool early,
+                                   cudaStream_t s);
 // The step without clip, staged the same way (compile-time fold for N <= 8,
 // run-time fold beyond) where zero1_fused_staged holds: N <= 8, or N slab
 // tiles that fit shared memory with enough of them resident per SM to keep
@@ -129,9 +154,17 @@ cudaError_t launch_zero1_fused_tma(const Arena& a, const Avg& avg, const AdamArg
                                    bool store_avg, void* grads, float* master, float* m, float* v,
                                    void* weights, void* ws, cudaStream_t s);
 cudaError_t read_and_clear_pipeline_error(unsigned* flag);
-// Launch the staged AdamW kernel on a one-tile arena in `buf` (256 bytes)
-// with a barrier that never completes, so that its bounded wait runs out.
-cudaError_t launch_staged_timeout_selftest(void* buf, cudaStream_t s);
+// Launch one staged kernel (DPZ_SELFTEST_* of dpz.h) on the one-tile arena
+// laid out in `buf` (DPZ_SELFTEST_BUF_BYTES), with a barrier that never
+// completes and a short wait bound, so that its wait runs out; then the norm
+// finalisation where the kernel writes partials.
+cudaError_t launch_staged_timeout_selftest(int kernel, void* buf, cudaStream_t s);
+// The self-test's arena (N = 1, P = 8, bf16 gradients and weights) and its
+// layout in the buffer: the workspace at 0, norm_out, then gradients, master,
+// m, v and weights at +0, +32, +64, +96 and +128 from kSelftestGrads.
+constexpr Arena kSelftestArena{8, 8, 1, 1, 1};
+constexpr size_t kSelftestNormOut = 2560;
+constexpr size_t kSelftestGrads = 2816;
 // Counts the float inputs whose average division by N differs from an
 // IEEE division (the whole 2^32 pattern space).
 cudaError_t launch_selftest_division(const Avg& avg, unsigned long long* mismatches,
@@ -139,10 +172,35 @@ cudaError_t launch_selftest_division(const Avg& avg, unsigned long long* mismatc
 
 
 // The fixed device scratch of dp_grad_global_norm_static (norm_static.cu):
-// its size in bytes, and its device address on the current device (looked
-// up on the first call on each device).
+// its size in bytes, and its device address on the current device (looked up
+// on every call outside a stream capture on `s`, reused during one).
 size_t static_scratch_bytes();
-cudaError_t static_scratch_address(void** ptr);
+cudaError_t static_scratch_address(void** ptr, cudaStream_t s);
+
+#if defined(__CUDACC__)
+// Launch `kernel` on `s` through cudaLaunchKernelEx.  early: with
+// programmatic stream serialisation, so that the kernel may begin once every
+// block of the previous kernel on the stream has begun (and executed
+// griddepcontrol.launch_dependents) instead of once it has finished; the
+// kernel must then execute griddepcontrol.wait before it touches anything
+// that earlier work writes or reads.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, bool early, Args... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = early ? attr : nullptr;
+    cfg.numAttrs = early ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+#endif
 
 // Name of the kernel the last launcher call on this thread launched.
 const char* last_kernel_name();

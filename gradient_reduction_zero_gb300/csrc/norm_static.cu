@@ -10,7 +10,7 @@
 // ordering between them) therefore race on the same scratch.
 #include <cuda_runtime.h>
 
-#include <mutex>
+#include <atomic>
 
 #include "internal.h"
 
@@ -21,8 +21,9 @@ namespace {
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;   // 4 MiB
 constexpr int kMaxDevices = 256;
 
-std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
+// The array's device address per device, from the last call outside a stream
+// capture on that device.
+std::atomic<void*> g_addr[kMaxDevices];
 
 }  // namespace
 
@@ -31,22 +32,34 @@ static __device__ __align__(256) unsigned char g_norm_scratch[kStaticScratchByte
 size_t static_scratch_bytes() { return kStaticScratchBytes; }
 
 // The array's device address on the current device.  In host code the name
-// g_norm_scratch is only a stand-in for the symbol, so the address is looked
-// up with cudaGetSymbolAddress, once per device, with that device current.
-cudaError_t static_scratch_address(void** ptr)
+// g_norm_scratch is only a stand-in for the symbol, so the address comes from
+// cudaGetSymbolAddress, with the device current.  It is looked up again on
+// every call that is not being captured into a CUDA graph (a device reset
+// loads the module anew, and the array may then sit elsewhere), and taken
+// from the last such lookup during a capture, where the lookup itself may not
+// be allowed; a capture before any uncaptured call on the device fails.
+cudaError_t static_scratch_address(void** ptr, cudaStream_t s)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_norm_scratch);
-        if (e != cudaSuccess) return e;
-        g_addr[dev] = p;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();     // the query's own error is not the caller's
+        cs = cudaStreamCaptureStatusActive;
     }
-    *ptr = g_addr[dev];
+    if (cs != cudaStreamCaptureStatusNone) {
+        void* p = g_addr[dev].load(std::memory_order_acquire);
+        if (p == nullptr) return cudaErrorStreamCaptureUnsupported;
+        *ptr = p;
+        return cudaSuccess;
+    }
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_norm_scratch);
+    if (e != cudaSuccess) return e;
+    g_addr[dev].store(p, std::memory_order_release);
+    *ptr = p;
     return cudaSuccess;
 }
 

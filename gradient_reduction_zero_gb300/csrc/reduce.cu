@@ -7,6 +7,7 @@
 // 256-element segments (device.cuh): every thread of a warp works on the
 // same chunk (uniform ring order) and consecutive lanes touch consecutive 16-
 // or 32-byte words of every slab (coalesced).
+#include "bulk.cuh"
 #include "device.cuh"
 #include "internal.h"
 
@@ -147,6 +148,7 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
     const int64_t groups = C / kGroup;
     const int64_t segs = segments_per_chunk(C);
     const int lane = threadIdx.x & 31;
+    if (SUMSQ) pdl_launch_dependents();       // the norm finalisation may launch (it waits)
     if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     if constexpr (ReduceSegsPerWarp<GDT, NT, ALL>::value > 1) {
         reduce_segments<GDT, NT, ALL, SUMSQ, ReduceSegsPerWarp<GDT, NT, ALL>::value>(
@@ -219,6 +221,7 @@ k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restric
     const int64_t segs = segments_per_chunk(C);
     const int lane = threadIdx.x & 31;
     const int64_t sslab = src_stride * ES;
+    if (SUMSQ) pdl_launch_dependents();       // the norm finalisation may launch (it waits)
     if (SUMSQ && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     const int c = c_first + (int)blockIdx.y;
     const int64_t plo = lo > c * C ? lo : c * C;
@@ -264,25 +267,73 @@ struct StreamSegs {
     static constexpr int value = DT == 0 ? 2 : 4;
 };
 
+// Status bits a partial (or a first-stage sum) stands for: none for a sum of
+// squares, which is never negative; DPZ_STATUS_NORM_SKIPPED for
+// kPartialNormSkipped; both bits for kPartialStepSkipped.
+__device__ __forceinline__ unsigned marker_bits(double x)
+{
+    return (x < 0.0 ? DPZ_STATUS_NORM_SKIPPED : 0u) |
+           (x < 0.5 * (kPartialNormSkipped + kPartialStepSkipped) ? DPZ_STATUS_UPDATE_SKIPPED : 0u);
+}
+
+// The block-wide OR of the threads' status bits (contains __syncthreads()).
+__device__ __forceinline__ unsigned block_or_bits(unsigned b)
+{
+    const unsigned norm = __syncthreads_or(b & DPZ_STATUS_NORM_SKIPPED) ? DPZ_STATUS_NORM_SKIPPED : 0u;
+    const unsigned upd =
+        __syncthreads_or(b & DPZ_STATUS_UPDATE_SKIPPED) ? DPZ_STATUS_UPDATE_SKIPPED : 0u;
+    return norm | upd;
+}
+
 // Sum of the n segment partials in a fixed order, independent of the device:
 // block b of F adds the contiguous range [b*L, (b+1)*L) (L = ceil(n/F)) into
 // stage1[b]; the last block to arrive (an arrival counter, not an ordering)
-// adds stage1[0..F-1] and writes sumsq, the norm and *norm_out.  No block
-// waits for another.
+// adds stage1[0..F-1] and writes sumsq, the norm, the status word and
+// *norm_out.  No block waits for another.  Each thread adds its terms i,
+// i + 512, ... strictly in that order; the loads of eight consecutive terms
+// are issued before their adds, so the latency of one load is paid once per
+// eight terms.  A partial that is a skipped tile's marker makes the norm NaN
+// and sets the status bits the marker stands for.
+//
+// The kernel is launched early behind the kernel that writes the partials
+// (programmatic dependent launch): it lets the update that follows launch
+// early in turn, then waits for the partials.
 __global__ void __launch_bounds__(kFinalThreads)
 k_norm_finalize(WsHeader* __restrict__ hdr, double* __restrict__ stage1,
                 const double* __restrict__ partials, int64_t n, float* __restrict__ norm_out)
 {
+    pdl_launch_dependents();
+    pdl_wait_prior();
     const int F = gridDim.x;
     const int64_t L = (n + F - 1) / F;
     const int64_t lo = (int64_t)blockIdx.x * L;
     const int64_t hi = lo + L < n ? lo + L : n;
+    const int64_t bd = blockDim.x;
     double v = 0.0;
-    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) v += partials[i];
+    unsigned bits = 0;
+    int64_t i = lo + threadIdx.x;
+    for (; i + 7 * bd < hi; i += 8 * bd) {
+        double x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = __ldcg(&partials[i + k * bd]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            v += x[k];
+            bits |= marker_bits(x[k]);
+        }
+    }
+    for (; i < hi; i += bd) {
+        const double x = __ldcg(&partials[i]);
+        v += x;
+        bits |= marker_bits(x);
+    }
     v = block_sum(v);
+    bits = block_or_bits(bits);
     __shared__ bool is_last;
     if (threadIdx.x == 0) {
-        stage1[blockIdx.x] = v;
+        stage1[blockIdx.x] = (bits & DPZ_STATUS_UPDATE_SKIPPED) ? kPartialStepSkipped
+                             : bits                              ? kPartialNormSkipped
+                                                                 : v;
         __threadfence();
         const unsigned prev = atomicAdd(&hdr->arrive, 1u);
         is_last = prev == (unsigned)(F - 1);
@@ -291,13 +342,24 @@ k_norm_finalize(WsHeader* __restrict__ hdr, double* __restrict__ stage1,
     if (!is_last) return;
     __threadfence();
     double w = 0.0;
-    for (int i = threadIdx.x; i < F; i += blockDim.x) w += __ldcg(&stage1[i]);
+    unsigned wbits = 0;
+    for (int k = threadIdx.x; k < F; k += blockDim.x) {
+        const double x = __ldcg(&stage1[k]);
+        w += x;
+        wbits |= marker_bits(x);
+    }
     w = block_sum(w);
+    wbits = block_or_bits(wbits);
     if (threadIdx.x == 0) {
-        const float nrm = __double2float_rn(__dsqrt_rn(w));
+        float nrm = __double2float_rn(__dsqrt_rn(w));
+        if (wbits) {
+            w = __longlong_as_double(0x7ff8000000000000LL);
+            nrm = __int_as_float(0x7fc00000);
+        }
         hdr->sumsq = w;
         hdr->norm = nrm;
         hdr->nparts = (uint32_t)n;
+        hdr->status = wbits;
         hdr->arrive = 0u;
         if (norm_out) *norm_out = nrm;
     }
@@ -447,9 +509,8 @@ cudaError_t launch_norm_finalize(const Arena& a, void* ws, float* norm_out, cuda
     int64_t F = (n + 2047) / 2048;
     if (F > kFinalBlocks) F = kFinalBlocks;
     if (F < 1) F = 1;
-    k_norm_finalize<<<(int)F, kFinalThreads, 0, s>>>(static_cast<WsHeader*>(ws), ws_stage1(ws),
-                                                     ws_partials(ws), n, norm_out);
-    return cudaGetLastError();
+    return launch_kernel(k_norm_finalize, dim3((unsigned)F), dim3(kFinalThreads), 0, s, true,
+                         static_cast<WsHeader*>(ws), ws_stage1(ws), ws_partials(ws), n, norm_out);
 }
 
 cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s)

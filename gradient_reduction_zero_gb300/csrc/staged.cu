@@ -21,11 +21,17 @@
 //
 // Every wait on an mbarrier is bounded by the SM clock: if a tile has not
 // arrived after about two seconds the CTA sets the device error flag that
-// dpz_device_status reads, waits (again bounded) for its loads in flight, and
-// returns without writing.
-#include <map>
-#include <mutex>
-#include <utility>
+// dpz_device_status reads, reports the tile in the call's workspace (negative
+// markers in the tile's norm partials, which the finalisation turns into a
+// NaN norm and status bits; the update sets DPZ_STATUS_UPDATE_SKIPPED and a
+// NaN norm_out), waits (again bounded) for its loads in flight, and returns
+// without writing the tile.
+//
+// Kernel boundaries of the clipped step: the reduce kernel and the norm
+// finalisation let the next kernel launch early (griddepcontrol), and the
+// update issues its master/m/v loads before it waits for the finalisation, so
+// the first wave of the update streams while the finalisation runs.
+#include <atomic>
 
 #include "bulk.cuh"
 #include "device.cuh"
@@ -40,11 +46,13 @@ __device__ unsigned g_pipeline_error;
 
 // A tile whose loads did not arrive in time: raise the device flag and give
 // the loads (bounded) time to land, since shared memory must outlive them.
-__device__ __forceinline__ void abandon_tile(uint64_t* bar)
+__device__ __forceinline__ void abandon_tile(uint64_t* bar, long long limit)
 {
     atomicExch(&g_pipeline_error, 1u);
-    mbar_wait_bounded(bar);
+    mbar_wait_bounded(bar, limit);
 }
+
+__device__ __forceinline__ float quiet_nan() { return __int_as_float(0x7fc00000); }
 
 template <int GDT, int WDT>
 struct TmaTile {
@@ -56,17 +64,21 @@ struct TmaTile {
 };
 
 // grads: the averaged gradient of element e (chunk c) at grads + (c*avg_stride
-// + e) elements; hdr: the workspace header (the norm), read when clip > 0.
+// + e) elements; hdr: the workspace header (the norm, read when clip > 0; the
+// status word, where a skipped tile is reported; may be NULL without clip);
+// norm_out: set to NaN if this kernel gives up on a tile (may be NULL).
 // NT > 0: N == NT known at compile time; NT == 0: any N, read from n_rt.
-// extra_tx: bytes the barrier expects beyond the tile's loads, 0 except in
-// the self-test of the timeout path (dpz_selftest_staged_timeout), where the
-// barrier then never completes and the bounded wait runs out.
+// master/m/v are requested before griddepcontrol.wait, the averages and the
+// norm after it: launched early behind the finalisation (dp_zero1_step), the
+// kernel's first wave loads its state while the finalisation runs.
+// Ten CTAs per SM (at most 48 registers a thread), as many as the kernel
+// held before its early-launch prologue was added.
 template <int GDT, int WDT, int NT>
-__global__ void __launch_bounds__(kTmaThreads)
+__global__ void __launch_bounds__(kTmaThreads, 10)
 k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __restrict__ master,
                   float* __restrict__ mom, float* __restrict__ var, char* __restrict__ weights,
-                  int64_t P, int64_t C, int n_rt, AdamArgs h, const WsHeader* __restrict__ hdr,
-                  uint32_t extra_tx)
+                  int64_t P, int64_t C, int n_rt, AdamArgs h, WsHeader* __restrict__ hdr,
+                  float* __restrict__ norm_out, WaitSpec wait)
 {
     using GS = Group<GDT>;
     using WS = Group<WDT>;
@@ -90,17 +102,21 @@ k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __r
     if (tid == 0) {
         mbar_init_one(&full);
         timed_out = 0;
-        mbar_expect_tx(&full, (uint32_t)n * (GES + 12u) + extra_tx);
-        bulk_load(t.avg, grads + ((int64_t)c * avg_stride + e) * GES, (uint32_t)n * GES, &full);
+        mbar_expect_tx(&full, (uint32_t)n * (GES + 12u) + wait.extra_tx);
         bulk_load(t.th, master + e, (uint32_t)n * 4u, &full);
         bulk_load(t.m, mom + e, (uint32_t)n * 4u, &full);
         bulk_load(t.v, var + e, (uint32_t)n * 4u, &full);
     }
+    pdl_wait_prior();    // the averages and the norm are complete and visible
+    if (tid == 0)
+        bulk_load(t.avg, grads + ((int64_t)c * avg_stride + e) * GES, (uint32_t)n * GES, &full);
     __syncthreads();     // the barrier is initialised before anyone waits on it
 
     float scale = 1.0f;
-    bool do_scale = false;
+    bool do_scale = false, skip = false;
     if (h.clip > 0.0f) {
+        // a norm whose input was not read in full is unknown: no update at all
+        skip = (hdr->status & DPZ_STATUS_NORM_SKIPPED) != 0u;
         const float nrm = hdr->norm;
         if (nrm > h.clip) {
             scale = __fdiv_rn(h.clip, nrm);
@@ -108,10 +124,14 @@ k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __r
         }
     }
 
-    if (!mbar_wait_bounded(&full)) atomicExch(&timed_out, 1);
+    if (!mbar_wait_bounded(&full, wait.limit)) atomicExch(&timed_out, 1);
     __syncthreads();
-    if (timed_out) {
-        if (tid == 0) abandon_tile(&full);
+    if (timed_out || skip) {
+        if (tid == 0) {
+            if (timed_out) abandon_tile(&full, wait.limit);
+            if (hdr != nullptr) atomicOr(&hdr->status, DPZ_STATUS_UPDATE_SKIPPED);
+            if (timed_out && norm_out != nullptr) *norm_out = quiet_nan();
+        }
         return;
     }
 
@@ -185,8 +205,9 @@ __global__ void __launch_bounds__(TILE / kGroup)
 k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
                   float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C,
                   int n_rt, Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
-                  double* __restrict__ partials)
+                  double* __restrict__ partials, WaitSpec wait)
 {
+    pdl_launch_dependents();     // the norm finalisation may launch (it waits)
     using GS = Group<GDT>;
     using WS = Group<WDT>;
     constexpr int GES = GS::kBytes;
@@ -216,7 +237,7 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
     if (tid == 0) {
         mbar_init_one(&full);
         timed_out = 0;
-        mbar_expect_tx(&full, (uint32_t)n * ((uint32_t)nr * GES + 12u));
+        mbar_expect_tx(&full, (uint32_t)n * ((uint32_t)nr * GES + 12u) + wait.extra_tx);
 #pragma unroll
         for (int r = 0; r < nr; ++r)
             bulk_load(tg + r * kSlabTile, grads + r * gslab + e * GES, (uint32_t)n * GES, &full);
@@ -225,10 +246,15 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
         bulk_load(tv, var + e, (uint32_t)n * 4u, &full);
     }
     __syncthreads();     // the barrier is initialised before anyone waits on it
-    if (!mbar_wait_bounded(&full)) atomicExch(&timed_out, 1);
+    if (!mbar_wait_bounded(&full, wait.limit)) atomicExch(&timed_out, 1);
     __syncthreads();
     if (timed_out) {
-        if (tid == 0) abandon_tile(&full);
+        // the tile's partials say that neither its norm terms nor its update exist
+        const int seg = tid >> 5;
+        if (SUMSQ && lane == 0 && seg * kSegment < n)
+            partials[c * segments_per_chunk(C) + tc * (TILE / kSegment) + seg] =
+                kPartialStepSkipped;
+        if (tid == 0) abandon_tile(&full, wait.limit);
         return;
     }
 
@@ -313,8 +339,9 @@ constexpr int kNormThreads = 256;
 template <int GDT>
 __global__ void __launch_bounds__(kNormThreads)
 k_norm_owned_tma(const char* __restrict__ grads, int64_t P, int64_t C,
-                 WsHeader* __restrict__ hdr, double* __restrict__ partials)
+                 WsHeader* __restrict__ hdr, double* __restrict__ partials, WaitSpec wait)
 {
+    pdl_launch_dependents();     // the norm finalisation may launch (it waits)
     constexpr int ES = Group<GDT>::kBytes;
     constexpr int T = kNormTileBytes / ES;            // elements per tile, a multiple of 256
     extern __shared__ __align__(128) unsigned char dsmem[];
@@ -333,18 +360,21 @@ k_norm_owned_tma(const char* __restrict__ grads, int64_t P, int64_t C,
     if (tid == 0) {
         mbar_init_one(&full);
         timed_out = 0;
-        mbar_expect_tx(&full, (uint32_t)n * ES);
+        mbar_expect_tx(&full, (uint32_t)n * ES + wait.extra_tx);
         bulk_load(dsmem, grads + ((int64_t)c * P + e) * ES, (uint32_t)n * ES, &full);
     }
     __syncthreads();
-    if (!mbar_wait_bounded(&full)) atomicExch(&timed_out, 1);
-    __syncthreads();
-    if (timed_out) {
-        if (tid == 0) abandon_tile(&full);
-        return;
-    }
     const int64_t segs = segments_per_chunk(C);
     const int nseg = (n + kSegment - 1) / kSegment;
+    if (!mbar_wait_bounded(&full, wait.limit)) atomicExch(&timed_out, 1);
+    __syncthreads();
+    if (timed_out) {
+        // the tile's partials say that its terms of the norm are missing
+        for (int sg = tid >> 5; sg < nseg; sg += kNormThreads / 32)
+            if (lane == 0) partials[c * segs + tc * (T / kSegment) + sg] = kPartialNormSkipped;
+        if (tid == 0) abandon_tile(&full, wait.limit);
+        return;
+    }
     for (int sg = tid >> 5; sg < nseg; sg += kNormThreads / 32) {      // whole warps
         const int i0 = sg * kSegment + lane * kGroup;
         float ss = 0.0f;
@@ -361,55 +391,69 @@ k_norm_owned_tma(const char* __restrict__ grads, int64_t P, int64_t C,
 
 namespace {
 
-std::mutex g_attr_mu;
-std::map<std::pair<int, const void*>, bool> g_attr_set;   // (device, kernel) done
+// Devices on which a kernel's dynamic shared memory limit has been raised,
+// one bit per device (0..255): each launcher keeps one of these per kernel,
+// so a launch after the first costs one atomic load.
+struct SmemRaised {
+    std::atomic<uint64_t> dev[4];
+};
 
 // Raise the kernel's dynamic shared memory limit on the current device, once.
-cudaError_t allow_smem(const void* fn, size_t smem)
+cudaError_t allow_smem(SmemRaised& done, const void* fn, size_t smem)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    int d = 0;
+    cudaError_t e = cudaGetDevice(&d);
     if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lk(g_attr_mu);
-    if (g_attr_set.count({dev, fn})) return cudaSuccess;
+    const bool cached = d >= 0 && d < 256;
+    const uint64_t bit = cached ? uint64_t(1) << (d & 63) : 0;
+    if (cached && (done.dev[d >> 6].load(std::memory_order_acquire) & bit)) return cudaSuccess;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) g_attr_set[{dev, fn}] = true;
+    if (e == cudaSuccess && cached) done.dev[d >> 6].fetch_or(bit, std::memory_order_release);
     return e;
 }
 
+// The arguments of one launch of the AdamW + all-gather kernel.
+struct UpdateLaunch {
+    const void* grads;
+    int64_t avg_stride;
+    float* master;
+    float* m;
+    float* v;
+    void* weights;
+    void* ws;
+    float* norm_out;
+    bool early;
+};
+
 template <int GDT, int WDT, int NT>
-cudaError_t tma_t(const Arena& a, const AdamArgs& h, const void* grads, int64_t avg_stride,
-                  float* master, float* m, float* v, void* weights, const void* ws,
-                  cudaStream_t s)
+cudaError_t tma_t(const Arena& a, const AdamArgs& h, const UpdateLaunch& u, cudaStream_t s)
 {
+    static SmemRaised raised;
     auto fn = k_adamw_bcast_tma<GDT, WDT, NT>;
     const size_t smem = sizeof(TmaTile<GDT, WDT>);
-    const cudaError_t e = allow_smem(reinterpret_cast<const void*>(fn), smem);
+    const cudaError_t e = allow_smem(raised, reinterpret_cast<const void*>(fn), smem);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (a.C + kTmaTile - 1) / kTmaTile * a.N;
     set_last_kernel_name("dpz_adamw_bcast");
-    fn<<<(unsigned)tiles, kTmaThreads, smem, s>>>(static_cast<const char*>(grads), avg_stride,
-                                                  master, m, v, static_cast<char*>(weights), a.P,
-                                                  a.C, a.N, h, static_cast<const WsHeader*>(ws),
-                                                  0u);
-    return cudaGetLastError();
+    return launch_kernel(fn, dim3((unsigned)tiles), dim3(kTmaThreads), smem, s, u.early,
+                         static_cast<const char*>(u.grads), u.avg_stride, u.master, u.m, u.v,
+                         static_cast<char*>(u.weights), a.P, a.C, a.N, h,
+                         static_cast<WsHeader*>(u.ws), u.norm_out, kWaitNormal);
 }
 
 template <int GDT, int WDT>
-cudaError_t tma_n(const Arena& a, const AdamArgs& h, const void* grads, int64_t avg_stride,
-                  float* master, float* m, float* v, void* weights, const void* ws,
-                  cudaStream_t s)
+cudaError_t tma_n(const Arena& a, const AdamArgs& h, const UpdateLaunch& u, cudaStream_t s)
 {
     switch (a.N) {
-    case 1: return tma_t<GDT, WDT, 1>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    case 2: return tma_t<GDT, WDT, 2>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    case 3: return tma_t<GDT, WDT, 3>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    case 4: return tma_t<GDT, WDT, 4>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    case 5: return tma_t<GDT, WDT, 5>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    case 6: return tma_t<GDT, WDT, 6>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    case 7: return tma_t<GDT, WDT, 7>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    case 8: return tma_t<GDT, WDT, 8>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    default: return tma_t<GDT, WDT, 0>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    case 1: return tma_t<GDT, WDT, 1>(a, h, u, s);
+    case 2: return tma_t<GDT, WDT, 2>(a, h, u, s);
+    case 3: return tma_t<GDT, WDT, 3>(a, h, u, s);
+    case 4: return tma_t<GDT, WDT, 4>(a, h, u, s);
+    case 5: return tma_t<GDT, WDT, 5>(a, h, u, s);
+    case 6: return tma_t<GDT, WDT, 6>(a, h, u, s);
+    case 7: return tma_t<GDT, WDT, 7>(a, h, u, s);
+    case 8: return tma_t<GDT, WDT, 8>(a, h, u, s);
+    default: return tma_t<GDT, WDT, 0>(a, h, u, s);
     }
 }
 
@@ -417,14 +461,15 @@ cudaError_t tma_n(const Arena& a, const AdamArgs& h, const void* grads, int64_t 
 
 cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
                                    int64_t avg_stride, float* master, float* m, float* v,
-                                   void* weights, const void* ws, cudaStream_t s)
+                                   void* weights, void* ws, float* norm_out, bool early,
+                                   cudaStream_t s)
 {
+    const UpdateLaunch u{grads, avg_stride, master, m, v, weights, ws, norm_out, early};
     const bool gbf = a.gdt != 0;       // stored averages: bf16 in both bf16 modes
-    if (gbf && a.wdt == 1)
-        return tma_n<1, 1>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    if (gbf) return tma_n<1, 0>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    if (a.wdt == 1) return tma_n<0, 1>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
-    return tma_n<0, 0>(a, h, grads, avg_stride, master, m, v, weights, ws, s);
+    if (gbf && a.wdt == 1) return tma_n<1, 1>(a, h, u, s);
+    if (gbf) return tma_n<1, 0>(a, h, u, s);
+    if (a.wdt == 1) return tma_n<0, 1>(a, h, u, s);
+    return tma_n<0, 0>(a, h, u, s);
 }
 
 // Shared memory of an SM (sm_103a), and what each resident CTA costs beyond
@@ -472,17 +517,19 @@ static cudaError_t fused_tma_t(const Arena& a, const Avg& avg, const AdamArgs& h
                                void* grads, float* master, float* m, float* v, void* weights,
                                void* ws, cudaStream_t s)
 {
+    static SmemRaised raised;
     auto fn = k_zero1_fused_tma<GDT, WDT, NT, SUMSQ, TILE>;
     const size_t smem = fold_tile_bytes(GDT, WDT, NT > 0 ? NT : a.N, TILE);
     // the run-time-N kernel may take any tile up to kFoldTileMaxBytes
-    const cudaError_t e = allow_smem(reinterpret_cast<const void*>(fn),
+    const cudaError_t e = allow_smem(raised, reinterpret_cast<const void*>(fn),
                                      NT > 0 ? smem : kFoldTileMaxBytes);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (a.C + TILE - 1) / TILE * a.N;
     set_last_kernel_name(SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused");
     fn<<<(unsigned)tiles, TILE / kGroup, smem, s>>>(
         static_cast<char*>(grads), master, m, v, static_cast<char*>(weights), a.P, a.C, a.N, avg,
-        h, store_avg ? 1 : 0, static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr);
+        h, store_avg ? 1 : 0, static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr,
+        kWaitNormal);
     return cudaGetLastError();
 }
 
@@ -559,13 +606,15 @@ cudaError_t launch_zero1_fused_tma(const Arena& a, const Avg& avg, const AdamArg
 template <int GDT>
 static cudaError_t norm_t(const Arena& a, const void* grads, void* ws, cudaStream_t s)
 {
+    static SmemRaised raised;
     auto fn = k_norm_owned_tma<GDT>;
-    const cudaError_t e = allow_smem(reinterpret_cast<const void*>(fn), kNormTileBytes);
+    const cudaError_t e = allow_smem(raised, reinterpret_cast<const void*>(fn), kNormTileBytes);
     if (e != cudaSuccess) return e;
     constexpr int T = kNormTileBytes / Group<GDT>::kBytes;
     const int64_t tiles = (a.C + T - 1) / T * a.N;
     fn<<<(unsigned)tiles, kNormThreads, kNormTileBytes, s>>>(
-        static_cast<const char*>(grads), a.P, a.C, static_cast<WsHeader*>(ws), ws_partials(ws));
+        static_cast<const char*>(grads), a.P, a.C, static_cast<WsHeader*>(ws), ws_partials(ws),
+        kWaitNormal);
     return cudaGetLastError();
 }
 
@@ -576,20 +625,31 @@ cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaS
     return a.gdt != 0 ? norm_t<1>(a, grads, ws, s) : norm_t<0>(a, grads, ws, s);
 }
 
-// The self-test of the timeout path: the staged AdamW kernel on a one-tile
-// arena (N = 1, P = 8, bf16 averages and weights, fp32 state) laid out in the
-// caller's buffer, with a barrier that expects 16 bytes more than the four
-// loads deliver.  Every copy it issues completes, so nothing is in flight
-// when the CTA gives up; the bounded wait runs out (about two seconds, then
-// the bounded wait of the abandon path), the device flag is set, and the
-// kernel returns without writing.
-cudaError_t launch_staged_timeout_selftest(void* buf, cudaStream_t s)
+// The self-test of the timeout path: one staged kernel on a one-tile arena
+// (N = 1, P = 8, bf16 gradients and weights, fp32 state) laid out in the
+// caller's buffer as dpz.h describes, with a barrier that expects 16 bytes
+// more than the kernel's loads deliver and a wait bound of
+// kSelftestWaitCycles.  Every copy it issues completes, so nothing is in
+// flight when the CTA gives up; the bounded wait runs out (and then the
+// bounded wait of the abandon path), the device flag is set, the tile is
+// reported in the workspace, and the kernel returns without writing the
+// arena.  The caller follows the norm and the step kernels with the
+// finalisation, which turns their markers into status bits and a NaN norm.
+constexpr long long kSelftestWaitCycles = 100000000LL;
+
+cudaError_t launch_staged_timeout_selftest(int kernel, void* buf, cudaStream_t s)
 {
-    auto fn = k_adamw_bcast_tma<1, 1, 1>;
-    const size_t smem = sizeof(TmaTile<1, 1>);
-    const cudaError_t e = allow_smem(reinterpret_cast<const void*>(fn), smem);
-    if (e != cudaSuccess) return e;
     char* b = static_cast<char*>(buf);
+    void* ws = b;
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    float* norm_out = reinterpret_cast<float*>(b + kSelftestNormOut);
+    char* grads = b + kSelftestGrads;
+    float* master = reinterpret_cast<float*>(b + kSelftestGrads + 32);
+    float* m = reinterpret_cast<float*>(b + kSelftestGrads + 64);
+    float* v = reinterpret_cast<float*>(b + kSelftestGrads + 96);
+    char* weights = b + kSelftestGrads + 128;
+    const Arena a = kSelftestArena;
+    const WaitSpec wait{kSelftestWaitCycles, 16u};
     AdamArgs h{};
     h.lr = 1e-3f;
     h.b1 = 0.9f;
@@ -599,11 +659,41 @@ cudaError_t launch_staged_timeout_selftest(void* buf, cudaStream_t s)
     h.bc1 = 0.1f;
     h.bc2 = 0.001f;
     h.eps = 1e-8f;
+    static_assert(kSelftestGrads + 144 <= DPZ_SELFTEST_BUF_BYTES, "the arena fits the buffer");
+    cudaError_t e = cudaSuccess;
+    if (kernel == DPZ_SELFTEST_UPDATE) {
+        static SmemRaised raised;
+        auto fn = k_adamw_bcast_tma<1, 1, 1>;
+        const size_t smem = sizeof(TmaTile<1, 1>);
+        e = allow_smem(raised, reinterpret_cast<const void*>(fn), smem);
+        if (e != cudaSuccess) return e;
+        set_last_kernel_name("dpz_selftest_staged_timeout");
+        fn<<<1, kTmaThreads, smem, s>>>(grads, a.P, master, m, v, weights, a.P, a.C, 1, h, hdr,
+                                       norm_out, wait);
+        return cudaGetLastError();
+    }
+    if (kernel == DPZ_SELFTEST_NORM) {
+        static SmemRaised raised;
+        auto fn = k_norm_owned_tma<1>;
+        e = allow_smem(raised, reinterpret_cast<const void*>(fn), kNormTileBytes);
+        if (e != cudaSuccess) return e;
+        fn<<<1, kNormThreads, kNormTileBytes, s>>>(grads, a.P, a.C, hdr, ws_partials(ws), wait);
+    } else if (kernel == DPZ_SELFTEST_STEP) {
+        static SmemRaised raised;
+        auto fn = k_zero1_fused_tma<1, 1, 1, true, kTmaTile>;
+        const size_t smem = fold_tile_bytes(1, 1, 1, kTmaTile);
+        e = allow_smem(raised, reinterpret_cast<const void*>(fn), smem);
+        if (e != cudaSuccess) return e;
+        Avg avg;
+        avg.fN = 1.0f;
+        avg.invN = 1.0f;
+        avg.pow2 = 1;
+        fn<<<1, kTmaThreads, smem, s>>>(grads, master, m, v, weights, a.P, a.C, 1, avg, h, 0, hdr,
+                                       ws_partials(ws), wait);
+    } else {
+        return cudaErrorInvalidValue;
+    }
     set_last_kernel_name("dpz_selftest_staged_timeout");
-    fn<<<1, kTmaThreads, smem, s>>>(b, 8, reinterpret_cast<float*>(b + 32),
-                                   reinterpret_cast<float*>(b + 64),
-                                   reinterpret_cast<float*>(b + 96), b + 128, 8, 8, 1, h,
-                                   nullptr, 16u);
     return cudaGetLastError();
 }
 

@@ -18,6 +18,9 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "dpz.h")
 F32, BF16, BF16_ACC32 = 0, 1, 2
 OK, ERR_INVALID_ARG, ERR_ALIGN, ERR_CUDA = 0, 1, 2, 3
 MAX_RANKS = 64
+# the per-call status word of a workspace (include/dpz.h)
+WS_STATUS_OFFSET = 20
+STATUS_NORM_SKIPPED, STATUS_UPDATE_SKIPPED = 1, 2
 
 
 class DpzError(RuntimeError):
@@ -69,7 +72,7 @@ _SIGS = {
     "dpz_version": ([], ctypes.c_char_p),
     "dpz_launch_count": ([], ctypes.c_int64),
     "dpz_device_status": ([ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
-    "dpz_selftest_staged_timeout": ([_VP, _VP], ctypes.c_int),
+    "dpz_selftest_staged_timeout": ([ctypes.c_int, _VP, _VP], ctypes.c_int),
     "dpz_selftest_average_division": ([ctypes.c_int, _VP, _VP], ctypes.c_int),
     "dpz_profile_start": ([ctypes.c_int], ctypes.c_int),
     "dpz_profile_stop": ([ctypes.POINTER(KernelStat), ctypes.c_int,
@@ -233,6 +236,47 @@ def dp_zero2_update(shards, master, m, v, weights, N: int, cfg: AdamWCfg, ws=Non
                                ctypes.byref(cfg), _ptr(ws), _stream_handle(stream)))
 
 
+class PreparedCall:
+    """One C-ABI call whose arguments were marshalled once: calling it makes
+    the same call again (the library validates the arguments and launches its
+    kernels every time).  For a training loop that runs the same step on the
+    same buffers, this leaves out the per-call Python work of turning tensors
+    into pointers and dtype codes.  It keeps the tensors and the AdamW
+    settings alive; changing a cfg field after preparing changes the calls."""
+    __slots__ = ("_fn", "_args", "_keep")
+
+    def __init__(self, fn, args, keep):
+        self._fn = fn
+        self._args = tuple(args)
+        self._keep = keep
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc != OK:
+            _check(rc)
+
+
+def _void_p(t):
+    return ctypes.c_void_p(_ptr(t))
+
+
+def prepare_zero1_step(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None,
+                       norm_out=None, stream=None, acc32: bool = False) -> PreparedCall:
+    """dp_zero1_step with its arguments marshalled once (PreparedCall)."""
+    args = (_void_p(grads), _void_p(master), _void_p(m), _void_p(v), _void_p(weights),
+            ctypes.c_int64(_np(grads, N)), ctypes.c_int(N), ctypes.c_int(dtype_code(grads, acc32)),
+            ctypes.c_int(dtype_code(weights)), ctypes.byref(cfg), _void_p(ws), _void_p(norm_out),
+            ctypes.c_void_p(_stream_handle(stream)))
+    return PreparedCall(lib.dp_zero1_step, args, (grads, master, m, v, weights, cfg, ws, norm_out))
+
+
+def prepare_allreduce_avg(grads, N: int, stream=None, acc32: bool = False) -> PreparedCall:
+    """dp_allreduce_avg with its arguments marshalled once (PreparedCall)."""
+    args = (_void_p(grads), ctypes.c_int64(_np(grads, N)), ctypes.c_int(N),
+            ctypes.c_int(dtype_code(grads, acc32)), ctypes.c_void_p(_stream_handle(stream)))
+    return PreparedCall(lib.dp_allreduce_avg, args, (grads,))
+
+
 def launch_count() -> int:
     return int(lib.dpz_launch_count())
 
@@ -245,17 +289,26 @@ def device_status() -> int:
     return f.value
 
 
-SELFTEST_BUF_BYTES = 256
+def ws_status(ws) -> int:
+    """The DPZ_STATUS_* bits of a workspace tensor's status word (a read of
+    device memory; it synchronises with the current stream)."""
+    return int(ws[WS_STATUS_OFFSET:WS_STATUS_OFFSET + 4].view(_torch().int32).item())
 
 
-def selftest_staged_timeout(buf, stream=None) -> None:
-    """Launch the staged AdamW kernel on a one-tile arena in `buf` (a device
-    tensor of at least SELFTEST_BUF_BYTES bytes) with a barrier that never
-    completes, so that its bounded wait runs out and sets the device flag
-    (about four seconds)."""
+SELFTEST_BUF_BYTES = 4096
+SELFTEST_UPDATE, SELFTEST_NORM, SELFTEST_STEP = 0, 1, 2
+# offsets in the self-test buffer (include/dpz.h)
+SELFTEST_NORM_OUT, SELFTEST_GRADS = 2560, 2816
+
+
+def selftest_staged_timeout(kernel: int, buf, stream=None) -> None:
+    """Launch one staged kernel (SELFTEST_*) on the one-tile arena laid out in
+    `buf` (a 256-byte aligned device tensor of at least SELFTEST_BUF_BYTES
+    bytes) with a barrier that never completes and a short wait bound, so
+    that the kernel gives up on its tile and reports it."""
     if buf.numel() * buf.element_size() < SELFTEST_BUF_BYTES:
         raise ValueError(f"buf must hold at least {SELFTEST_BUF_BYTES} bytes")
-    _check(lib.dpz_selftest_staged_timeout(_ptr(buf), _stream_handle(stream)))
+    _check(lib.dpz_selftest_staged_timeout(int(kernel), _ptr(buf), _stream_handle(stream)))
 
 
 def selftest_average_division(N: int, counter, stream=None) -> None:

@@ -93,6 +93,35 @@ extern "C" {
 
 #define DPZ_MAX_RANKS 64
 
+/* Per-call status in the workspace.  Three kernels stage their tiles through
+ * shared memory with asynchronous bulk copies and wait for them on a barrier,
+ * bounded by the SM clock (about two seconds): the norm of the owner chunks
+ * (dp_grad_global_norm, dp_grad_global_norm_static), the one-kernel step
+ * without clip (dp_zero1_step), and the AdamW + all-gather update from stored
+ * averages (dp_zero1_step with clip, dp_zero1_update, dp_zero2_update).  If a
+ * wait runs out the kernel gives up on that tile instead of hanging, and says
+ * so in stream order, for a consumer on the same stream to see without
+ * synchronising:
+ *   - the uint32 at byte DPZ_WS_STATUS_OFFSET of the call's workspace holds
+ *     DPZ_STATUS_* bits.  Every norm finalisation (dp_grad_global_norm,
+ *     dp_grad_norm_finalize, dp_zero1_step with clip or with norm_out) writes
+ *     the whole word; the update kernels that follow it only set
+ *     DPZ_STATUS_UPDATE_SKIPPED.  So after dp_zero1_step with a workspace and
+ *     a clip or a norm_out, and after dp_grad_norm_finalize followed by
+ *     dp_zero1_update / dp_zero2_update, the word describes that step alone;
+ *   - the norm written to the workspace and to norm_out is NaN;
+ *   - an update with clipping whose norm has DPZ_STATUS_NORM_SKIPPED set is not
+ *     applied at all: master/m/v and the weights keep their values and
+ *     DPZ_STATUS_UPDATE_SKIPPED is set.
+ * dp_zero1_step without clip and without norm_out runs no finalisation and
+ * has no per-call word; there, and in every case, the device-wide flag of
+ * dpz_device_status is raised as well.  NaN or Inf in the data is not a
+ * status: it propagates into the norm and the update as any value does. */
+#define DPZ_WS_STATUS_OFFSET 20
+#define DPZ_STATUS_NORM_SKIPPED 1u   /* a tile of the norm's input was not read */
+#define DPZ_STATUS_UPDATE_SKIPPED 2u /* a tile of master/m/v and the weights was
+                                        not updated (it keeps the old values) */
+
 /* AdamW hyperparameters for one step (A4 Part 4: the optimizer runs on the
  * owned shard).  The update, in fp32 with every operation rounded:
  *   g  = avg * s          s = clip/norm if clip_norm > 0 and norm > clip_norm,
@@ -285,33 +314,44 @@ DPZ_API const char* dpz_last_error(void);
 /* Library version string. */
 DPZ_API const char* dpz_version(void);
 
-/* Device-side error flag of the current device, read and cleared.  Two
- * kernels stage their tiles through shared memory with asynchronous bulk
- * copies and wait for them on a barrier: the AdamW + all-gather kernel that
- * reads stored averages (dp_zero1_step with clipping, dp_zero1_update,
- * dp_zero2_update) and the norm of the owner chunks (dp_grad_global_norm,
- * dp_grad_global_norm_static).  That wait is bounded by the SM clock (about
- * two seconds); if it runs out, the tile is left unprocessed and this flag is
- * set, instead of the kernel hanging.  *flag_out = 1 if that happened since the last call, else 0.
- * Synchronous: call it after the work in question has finished (for example
- * after cudaStreamSynchronize), not inside a stream capture.  Returns
- * DPZ_ERR_INVALID_ARG for a NULL flag_out, DPZ_ERR_CUDA if the read fails. */
+/* Device-side error flag of the current device, read and cleared: 1 if any
+ * bulk-copy staged kernel (see DPZ_WS_STATUS_OFFSET) gave up on a tile since
+ * the last call, else 0.  Synchronous: call it after the work in question has
+ * finished (for example after cudaStreamSynchronize), not inside a stream
+ * capture.  Returns DPZ_ERR_INVALID_ARG for a NULL flag_out, DPZ_ERR_CUDA if
+ * the read fails. */
 DPZ_API int dpz_device_status(int* flag_out);
 
-/* Self-test of the timeout path behind dpz_device_status (no counterpart on
- * the pages).  Launches, on `stream`, the staged AdamW + all-gather kernel on
- * a one-tile arena laid out in `buf`: DPZ_SELFTEST_BUF_BYTES bytes of caller
- * device memory, 16-byte aligned (bf16 averages at +0, fp32 master/m/v at
- * +32/+64/+96, bf16 weights at +128, 8 elements each).  Its barrier expects
- * 16 bytes more than its bulk loads deliver; every copy it issues completes,
- * so the wait runs out, after about two seconds plus the abandon path's
- * bounded wait.  The kernel then sets the device flag and returns without
- * writing `buf`.  After synchronising, dpz_device_status reports 1 and the
- * context is usable.  Returns DPZ_ERR_INVALID_ARG for a NULL buf,
- * DPZ_ERR_ALIGN for one not 16-byte aligned, DPZ_ERR_CUDA if the launch
+/* Self-test of the timeout path (no counterpart on the pages).  Launches, on
+ * `stream`, one of the staged kernels on a one-tile arena (N = 1, P = 8) laid
+ * out in `buf`, DPZ_SELFTEST_BUF_BYTES bytes of caller device memory, 256-byte
+ * aligned:
+ *   +0     the arena's workspace (DPZ_WS_STATUS_OFFSET is relative to it)
+ *   +2560  norm_out, one float
+ *   +2816  gradients (bf16, 8 elements); +2848, +2880, +2912 master, m, v
+ *          (fp32, 8 each); +2944 weights (bf16, 8)
+ * The kernel's barrier expects 16 bytes more than its bulk loads deliver and
+ * its wait is bounded by about 10^8 SM cycles (some 0.05 to 0.1 s) instead of
+ * the usual two seconds.  Every copy it issues completes, so the wait runs out
+ * and nothing is in flight when the kernel gives up.  kernel:
+ *   DPZ_SELFTEST_UPDATE  the AdamW + all-gather update (without clip): sets
+ *                        DPZ_STATUS_UPDATE_SKIPPED in the workspace's status
+ *                        word and NaN in norm_out;
+ *   DPZ_SELFTEST_NORM    the norm of the owner chunks, then the finalisation:
+ *                        status DPZ_STATUS_NORM_SKIPPED, norm_out NaN;
+ *   DPZ_SELFTEST_STEP    the step without clip with norm partials, then the
+ *                        finalisation: status NORM_SKIPPED | UPDATE_SKIPPED,
+ *                        norm_out NaN.
+ * No kernel writes the arena's gradients, master/m/v or weights, and each
+ * raises the device flag of dpz_device_status; the context stays usable.
+ * Returns DPZ_ERR_INVALID_ARG for a NULL buf or an unknown kernel,
+ * DPZ_ERR_ALIGN for a buf not 256-byte aligned, DPZ_ERR_CUDA if a launch
  * fails. */
-#define DPZ_SELFTEST_BUF_BYTES 256
-DPZ_API int dpz_selftest_staged_timeout(void* buf, void* stream);
+#define DPZ_SELFTEST_BUF_BYTES 4096
+#define DPZ_SELFTEST_UPDATE 0
+#define DPZ_SELFTEST_NORM 1
+#define DPZ_SELFTEST_STEP 2
+DPZ_API int dpz_selftest_staged_timeout(int kernel, void* buf, void* stream);
 
 /* Self-test of the division inside the average (no counterpart on the pages,
  * which fix only that the reduced sum is divided by N).  For N not a power of

@@ -3,6 +3,7 @@ header declares, and rejects bad arguments before any CUDA call."""
 import ctypes
 import importlib.util
 import os
+import re
 import subprocess
 import sys
 
@@ -168,8 +169,35 @@ def test_device_status_rejects_null(dpz):
 
 
 def test_selftest_rejects_bad_buffer(dpz):
-    assert dpz.lib.dpz_selftest_staged_timeout(None, None) == 1
-    assert dpz.lib.dpz_selftest_staged_timeout(A + 8, None) == 2        # misaligned
+    for k in (dpz.SELFTEST_UPDATE, dpz.SELFTEST_NORM, dpz.SELFTEST_STEP):
+        assert dpz.lib.dpz_selftest_staged_timeout(k, None, None) == 1
+        assert dpz.lib.dpz_selftest_staged_timeout(k, A + 16, None) == 2   # not 256-aligned
+    assert dpz.lib.dpz_selftest_staged_timeout(3, A, None) == 1            # no such kernel
+    assert b"kernel" in dpz.lib.dpz_last_error()
+
+
+def test_header_constants_match_binding(dpz):
+    """The status word's offset and bits, and the self-test's layout, as the
+    header declares them."""
+    text = open(dpz.HEADER).read()
+
+    def define(name):
+        m = re.search(r"#define\s+" + name + r"\s+(\d+)", text)
+        assert m, name
+        return int(m.group(1))
+
+    assert define("DPZ_WS_STATUS_OFFSET") == dpz.WS_STATUS_OFFSET
+    assert define("DPZ_STATUS_NORM_SKIPPED") == dpz.STATUS_NORM_SKIPPED
+    assert define("DPZ_STATUS_UPDATE_SKIPPED") == dpz.STATUS_UPDATE_SKIPPED
+    assert define("DPZ_SELFTEST_BUF_BYTES") == dpz.SELFTEST_BUF_BYTES
+    assert [define(f"DPZ_SELFTEST_{k}") for k in ("UPDATE", "NORM", "STEP")] == \
+        [dpz.SELFTEST_UPDATE, dpz.SELFTEST_NORM, dpz.SELFTEST_STEP]
+    assert f"+{dpz.SELFTEST_NORM_OUT}  norm_out" in text
+    assert f"+{dpz.SELFTEST_GRADS}  gradients" in text
+    # the status word follows the header's double, float and three uint32
+    assert dpz.WS_STATUS_OFFSET == 8 + 4 + 4 + 4
+    # the self-test arena's workspace fits before norm_out
+    assert dpz.lib.dpz_workspace_bytes(8, 1) <= dpz.SELFTEST_NORM_OUT
 
 
 def test_division_selftest_rejects_bad_args(dpz):
