@@ -82,3 +82,37 @@ def assert_close_tol(gpu, ref, tol, what):
     assert np.array_equal(np.isnan(g), nan), f"{what}: NaN positions differ"
     bad = np.abs(g[~nan] - r[~nan]) > tol[~nan]
     assert not bad.any(), f"{what}: {bad.sum()} elements outside tolerance"
+
+
+def check_step(w, g, th, m, v, wts, out, check_avg=True, acc32=False):
+    """One GPU step `out` = (grads, master, m, v, weights, norm) against the
+    oracle's zero1_step on the same inputs: the averaged owner chunks bit for
+    bit (check_avg), the norm within relative 1e-6 (norm < 0: not asked for),
+    and master/m/v and the weights bit for bit when the two norms are the same
+    float (always without clip), else within the stated tolerances."""
+    Gg, Tg, Mg, Vg, Wg, gnorm = out
+    cfg = O.cfg_from_workload(w)
+    G, T, M, V, W = g.copy(), th.copy(), m.copy(), v.copy(), wts.copy()
+    onorm, oscale, _, _ = O.zero1_step(G, T, M, V, W, cfg, acc32=acc32)
+    C = w.C
+    if gnorm >= 0:
+        assert abs(gnorm - onorm) <= 1e-6 * onorm, (gnorm, onorm)
+    if check_avg:
+        for c in range(w.N):
+            sl = slice(c * C, (c + 1) * C)
+            assert same_bits(Gg[c, sl], G[c, sl]), f"averaged chunk {c}"
+    exact = w.clip <= 0 or gnorm == onorm
+    if exact:
+        assert same_bits(Tg, T) and same_bits(Mg, M) and same_bits(Vg, V)
+        assert same_bits(Wg, W)
+        return
+    avg = np.concatenate([f32_view(G[c, c * C:(c + 1) * C]) for c in range(w.N)])
+    tm, tv, tt = state_tolerances(avg, oscale, th, m, v, M, V, cfg)
+    assert_close_tol(Mg, M, tm, "m")
+    assert_close_tol(Vg, V, tv, "v")
+    assert_close_tol(Tg, T, tt, "master")
+    if Wg.dtype == np.uint16:
+        assert_weights(Wg, W, exact=False)
+    else:
+        for r in range(w.N):
+            assert_close_tol(Wg[r], W[r], tt, "weights")

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import gradient_reduction_zero_gb300.dpz as dpz
-    from gpu_util import DEV, down, same_bits, up
+    from gpu_util import DEV, check_step, down, same_bits, up
 
 
 def segment_buckets(P, N, nb, seed):
@@ -89,9 +89,13 @@ def test_bucketed_zero1_matches_whole_arena(N, C, nb, clip, acc32, max_ctas):
     for c in range(N):
         sl = slice(c * C, (c + 1) * C)
         assert same_bits(Gd[c, sl], ref[0][c, sl])
-    for got, want in zip((down(T), down(M), down(V), down(W)), ref[1:5]):
-        assert same_bits(got, want)
+    out = (Gd.reshape(N, P), down(T), down(M), down(V), down(W).reshape(N, P), nrm.item())
+    for got, want in zip(out[1:5], ref[1:5]):
+        assert same_bits(got.reshape(want.shape), want)
     assert nrm.item() == ref[5]
+    assert dpz.ws_status(ws) == 0
+    # and directly against the oracle's step on the same inputs
+    check_step(w, g, th, m, v, np.zeros((N, P), dtype=np.uint16), out, acc32=acc32)
 
 
 @pytest.mark.parametrize("N,C,nb", [(4, 6152, 7), (8, 2056, 5), (3, 1000, 4), (4, 262_144, 12)])
@@ -133,13 +137,17 @@ def test_zero2_matches_zero1(N, C, nb, clip, acc32, max_ctas):
     torch.cuda.synchronize()
     owner_avg = np.concatenate([ref[0][c, c * C:(c + 1) * C] for c in range(N)])
     assert same_bits(down(shards), owner_avg)
-    for got, want in zip((down(T), down(M), down(V), down(W)), ref[1:5]):
-        assert same_bits(got, want)
+    out = (None, down(T), down(M), down(V), down(W).reshape(N, P), nrm.item())
+    for got, want in zip(out[1:5], ref[1:5]):
+        assert same_bits(got.reshape(want.shape), want)
     assert nrm.item() == ref[5]
-    # the shards are the oracle's reduce-scatter, and the step its ZeRO-1 step
+    assert dpz.ws_status(ws) == 0
+    # the shards are the oracle's reduce-scatter, and the update its ZeRO-1 step
     a = g.copy()
     O.reduce_scatter_avg(a, acc32=acc32)
     assert same_bits(down(shards), np.concatenate([a[c, c * C:(c + 1) * C] for c in range(N)]))
+    check_step(w, g, th, m, v, np.zeros((N, P), dtype=np.uint16), out, check_avg=False,
+               acc32=acc32)
 
 
 def test_range_without_partials_any_alignment():

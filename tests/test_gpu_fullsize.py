@@ -1,14 +1,14 @@
-"""GPU parity at the workloads' full sizes, in the launch configurations the
-benchmark times (dp_zero1_step with clip, workspace and norm output; also
-without clip, the one-kernel step, and with the fp32-accumulating ring;
-dp_allreduce_avg for the all-reduce workloads).  The oracle computes sampled
-windows of every chunk one by one (the start, the middle and the ragged end)
-and the global norm over the whole arena, window by window on host threads;
-the rest is checked through properties that hold at any size (non-owner
-chunks untouched, every weight replica identical)."""
+"""GPU parity at the workloads' full sizes, on every element, in the launch
+configurations the benchmark times (dp_zero1_step with clip, workspace and
+norm output; also without clip, the one-kernel step, and with the
+fp32-accumulating ring; dp_allreduce_avg for the all-reduce workloads).
+
+The oracle runs window by window (oracle_windows): the windows tile every
+chunk, so every averaged gradient, every untouched non-owner element, every
+master/m/v value and every weight of every replica is compared.  Host threads
+run the oracle on the windows while the matching device windows are copied
+down, so host memory stays bounded (a few hundred MB per thread)."""
 import math
-import os
-from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
@@ -16,6 +16,7 @@ import torch
 
 import inputs as I
 import oracle as O
+from oracle_windows import for_every_window, oracle_full_sumsq, remember_sumsq
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -24,28 +25,22 @@ if torch.cuda.is_available():
     from gpu_util import (DEV, assert_close_tol, assert_weights, down, f32_view, same_bits,
                           state_tolerances)
 
-WIDTH = 4096
+
+def first_difference(got, want):
+    """Index and values of the first element whose bits differ (NaN matches
+    NaN)."""
+    fa, fb = f32_view(got).ravel(), f32_view(want).ravel()
+    ia = got.ravel().view(np.uint16 if got.dtype == np.uint16 else np.uint32)
+    ib = want.ravel().view(np.uint16 if want.dtype == np.uint16 else np.uint32)
+    bad = (ia != ib) & ~(np.isnan(fa) & np.isnan(fb))
+    i = int(np.argmax(bad))
+    return i, fa[i], fb[i]
 
 
-def window_offsets(C):
-    return sorted({0, (C // 2) // 8 * 8, C - WIDTH})
-
-
-def oracle_full_sumsq(w, width=1 << 20, acc32=False):
-    """Sum of squares of the averaged gradient of the whole arena: the oracle's
-    reduce-scatter, average and sum of squares on every window, added with
-    math.fsum (the sum of squares is additive over windows)."""
-    C = w.C
-
-    def part(o):
-        wd = min(width, C - o)
-        g = I.window_arena_host(w, o, wd)
-        O.reduce_scatter_avg(g, acc32=acc32)
-        return O.sumsq_owned(g)
-
-    with ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
-        parts = list(ex.map(part, range(0, C, width)))
-    return math.fsum(parts)
+def assert_same(got, want, what):
+    if not same_bits(got, want):
+        i, a, b = first_difference(got, want)
+        raise AssertionError(f"{what}: element {i} of the window differs (gpu {a}, oracle {b})")
 
 
 def gpu_window(t, N, P, C, o, wd):
@@ -58,13 +53,15 @@ def gpu_state_window(t, N, C, o, wd):
     return np.concatenate([down(t[c * C + o:c * C + o + wd]) for c in range(N)])
 
 
-@pytest.mark.parametrize("w,acc32", [(I.GPT2_124M, False), (I.GPT2_1P5B, False),
+@pytest.mark.parametrize("w,acc32", [(I.GPT2_124M, False),
                                      (I.GPT2_1P5B.with_(clip=0.0), False),
+                                     (I.GPT2_1P5B, False),
                                      (I.GPT2_124M, True)],
-                         ids=["gpt2-124m", "gpt2-1.5b", "gpt2-1.5b-no-clip", "gpt2-124m-acc32"])
+                         ids=["gpt2-124m", "gpt2-1.5b-no-clip", "gpt2-1.5b", "gpt2-124m-acc32"])
 def test_zero1_step_full_size(w, acc32):
     """The clipped three-kernel step, the one-kernel step without clipping,
-    and the fp32-accumulating ring, at full size."""
+    and the fp32-accumulating ring, at full size, every element against the
+    oracle."""
     N, P, C = w.N, w.P, w.C
     gd = torch.bfloat16
     G = torch.empty(N * P, dtype=gd, device=DEV)
@@ -81,69 +78,88 @@ def test_zero1_step_full_size(w, acc32):
     dpz.dp_zero1_step(G, T, M, V, W, N, cfg, ws=ws, norm_out=nrm, acc32=acc32)
     torch.cuda.synchronize()
     gnorm = nrm.item()
+    assert dpz.ws_status(ws) == 0
     # the standalone norm (bulk-copy staged kernel) of the stored averages is
     # the same float: the same per-segment partials, summed in the same order
     ws2, nrm2 = dpz.workspace(P, N, DEV), torch.zeros(1, device=DEV)
     dpz.dp_grad_global_norm(G, N, ws2, nrm2)
     torch.cuda.synchronize()
     assert nrm2.item() == gnorm
+    assert dpz.ws_status(ws2) == 0
     assert dpz.device_status() == 0
     del ws2
 
-    ss = oracle_full_sumsq(w, acc32=acc32)
-    onorm, oscale = O.clip_scale(ss, w.clip)
-    assert abs(gnorm - onorm) <= 1e-6 * onorm, (gnorm, onorm)
-    if w.clip > 0:
-        assert oscale < 1.0                       # the clip is active
-
+    # without clipping the update does not depend on the norm, so the windows
+    # run in one pass that also yields the sum of squares; with clipping the
+    # oracle needs the whole arena's sum of squares first
+    ss = oracle_full_sumsq(w, acc32) if w.clip > 0 else None
+    onorm, oscale = O.clip_scale(ss, w.clip) if ss is not None else (None, 1.0)
+    exact = w.clip <= 0 or gnorm == onorm
     ocfg = O.cfg_from_workload(w)
-    for o in window_offsets(C):
-        g = I.window_arena_host(w, o, WIDTH)
-        th = I.window_state_host(w, "master", o, WIDTH)
-        m = I.window_state_host(w, "m", o, WIDTH)
-        v = I.window_state_host(w, "v", o, WIDTH)
-        wt = np.zeros((N, N * WIDTH), dtype=np.uint16)
-        G1, T1, M1, V1, W1 = g.copy(), th.copy(), m.copy(), v.copy(), wt.copy()
-        n1, s1, _, _ = O.zero1_step(G1, T1, M1, V1, W1, ocfg, ext_sumsq=ss, acc32=acc32)
-        assert n1 == onorm
-        Gg = gpu_window(G, N, P, C, o, WIDTH)
-        Wg = gpu_window(W, N, P, C, o, WIDTH)
-        Tg = gpu_state_window(T, N, C, o, WIDTH)
-        Mg = gpu_state_window(M, N, C, o, WIDTH)
-        Vg = gpu_state_window(V, N, C, o, WIDTH)
+
+    def check(o, wd):
+        g = I.window_arena_host(w, o, wd)
+        th = I.window_state_host(w, "master", o, wd)
+        m = I.window_state_host(w, "m", o, wd)
+        v = I.window_state_host(w, "v", o, wd)
+        wt = np.zeros((N, N * wd), dtype=np.uint16)
+        G1, T1, M1, V1, W1 = g.copy(), th.copy(), m.copy(), v.copy(), wt
+        O.zero1_step(G1, T1, M1, V1, W1, ocfg, ext_sumsq=-1.0 if ss is None else ss,
+                     acc32=acc32)
+        Gg = gpu_window(G, N, P, C, o, wd)
+        Wg = gpu_window(W, N, P, C, o, wd)
+        Tg = gpu_state_window(T, N, C, o, wd)
+        Mg = gpu_state_window(M, N, C, o, wd)
+        Vg = gpu_state_window(V, N, C, o, wd)
         for c in range(N):
-            sl = slice(c * WIDTH, (c + 1) * WIDTH)
+            sl = slice(c * wd, (c + 1) * wd)
             for r in range(N):
-                want = G1[c, sl] if r == c else g[r, sl]    # owner: average; others: untouched
-                assert same_bits(Gg[r, sl], want), (o, r, c)
-        for r in range(N):
-            assert same_bits(Wg[r], Wg[0])
-        if gnorm == onorm or w.clip <= 0:
-            assert same_bits(Tg, T1) and same_bits(Mg, M1) and same_bits(Vg, V1)
-            assert same_bits(Wg, W1)
+                want = G1[c, sl] if r == c else g[r, sl]   # owner: average; others: untouched
+                assert_same(Gg[r, sl], want, f"grads slab {r} chunk {c} window {o}")
+        if exact:
+            assert_same(Tg, T1, f"master window {o}")
+            assert_same(Mg, M1, f"m window {o}")
+            assert_same(Vg, V1, f"v window {o}")
+            for r in range(N):
+                assert_same(Wg[r], W1[r], f"weights slab {r} window {o}")
         else:
-            avg = np.concatenate([f32_view(G1[c, c * WIDTH:(c + 1) * WIDTH]) for c in range(N)])
+            avg = np.concatenate([f32_view(G1[c, c * wd:(c + 1) * wd]) for c in range(N)])
             tm, tv, tt = state_tolerances(avg, oscale, th, m, v, M1, V1, ocfg)
             assert_close_tol(Mg, M1, tm, "m")
             assert_close_tol(Vg, V1, tv, "v")
             assert_close_tol(Tg, T1, tt, "master")
             assert_weights(Wg, W1, exact=False)
+        return O.sumsq_owned(G1)          # this window's part of the sum of squares
+
+    parts = for_every_window(C, check)
+    total = math.fsum(parts)
+    if ss is None:
+        remember_sumsq(w, acc32, total)
+        onorm, _ = O.clip_scale(total, 0.0)
+    else:
+        assert total == ss
+        assert oscale < 1.0                       # the clip is active
+    assert abs(gnorm - onorm) <= 1e-6 * onorm, (gnorm, onorm)
     del G, T, M, V, W
     torch.cuda.empty_cache()
 
 
 def _allreduce_full(w):
+    """dp_allreduce_avg on the whole arena; every element of every slab
+    against the oracle's ring all-reduce, window by window."""
     N, P, C = w.N, w.P, w.C
     G = torch.empty(N * P, dtype=torch.bfloat16 if w.gdtype == "bf16" else torch.float32,
                     device=DEV)
     I.fill_grads_device(w, G)
     dpz.dp_allreduce_avg(G, N)
     torch.cuda.synchronize()
-    wd = min(WIDTH, C)
-    for o in sorted({0, (C // 2) // 8 * 8, C - wd}):
+
+    def check(o, wd):
         g = I.window_arena_host(w, o, wd)
         O.ring_allreduce_avg(g)
-        assert same_bits(gpu_window(G, N, P, C, o, wd), g), o
+        assert_same(gpu_window(G, N, P, C, o, wd), g, f"all-reduce window {o}")
+
+    for_every_window(C, check)
     del G
     torch.cuda.empty_cache()
 
@@ -157,7 +173,7 @@ def test_allreduce_sweep(N):
     for size in I.SWEEP_SIZES:
         w = I.allreduce_sweep(size, N)
         if w.P <= 1 << 20:
-            # small enough for the whole arena
+            # small enough for the whole arena at once
             g = I.arena_host(w)
             G = torch.from_numpy(g.reshape(-1).copy()).to(DEV)
             dpz.dp_allreduce_avg(G, N)
@@ -188,9 +204,10 @@ def test_buckets_and_zero2_full_size():
     """The GPT-2 1.5B step in 16 buckets reduced on a side stream with the grid
     capped at one block per SM (the bench's overlap configuration), then the
     norm and dp_zero1_update; and as ZeRO-2 from a reused staging buffer into
-    gradient shards.  Both equal dp_zero1_step bit for bit: the same partials,
-    the same norm, the same averages, master/m/v and weights.  (dp_zero1_step
-    itself is checked against the oracle above.)"""
+    gradient shards.  Both equal dp_zero1_step bit for bit on every element:
+    the same partials, the same norm, the same averages, master/m/v and
+    weights.  (dp_zero1_step itself is compared with the oracle on every
+    element above.)"""
     w = I.GPT2_1P5B
     N, P, C = w.N, w.P, w.C
     sms = torch.cuda.get_device_properties(DEV).multi_processor_count
@@ -230,6 +247,7 @@ def test_buckets_and_zero2_full_size():
     main.wait_stream(comm)
     torch.cuda.synchronize()
     assert nrmb.item() == nrm.item()
+    assert dpz.ws_status(wsb) == 0
     owner_b = torch.cat([Gb.view(N, P)[c, c * C:(c + 1) * C] for c in range(N)])
     assert torch.equal(_bits(owner_b), _bits(owner))
     for got, want in ((Tb, T), (Mb, M), (Vb, V), (Wb, W)):
@@ -252,6 +270,7 @@ def test_buckets_and_zero2_full_size():
     dpz.dp_zero2_update(shards, T2, M2, V2, W2, N, cfg, ws=ws2)
     torch.cuda.synchronize()
     assert nrm2.item() == nrm.item()
+    assert dpz.ws_status(ws2) == 0
     assert torch.equal(_bits(shards), _bits(owner))
     for got, want in ((T2, T), (M2, M), (V2, V), (W2, W)):
         assert torch.equal(_bits(got), _bits(want))
@@ -264,8 +283,8 @@ def test_buckets_and_zero2_full_size():
 def test_graph_replay_full_size(clip):
     """The GPT-2 1.5B step captured in a CUDA graph (as bench --graph times it)
     and replayed twice equals two eager steps on a fresh copy of the inputs,
-    bit for bit: the calls only enqueue kernels, and every run of the step is
-    deterministic."""
+    bit for bit on every element: the calls only enqueue kernels, and every
+    run of the step is deterministic."""
     w = I.GPT2_1P5B.with_(clip=clip)
     N, P = w.N, w.P
     cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)

@@ -1,26 +1,28 @@
 """The step captured in a CUDA graph and replayed: the calls only enqueue
 kernels on the caller's stream (no allocation, no host synchronisation), so
-a captured step replays with the same bits as eager calls.  The tiny
-workload is launch-latency bound, which is where replaying a graph pays
-("Distributed training", "Overlap and graphs": one CUDA graph per GPU)."""
+a captured step replays with the same bits as eager calls, and its first
+replay is the oracle's step.  The tiny workload is launch-latency bound,
+which is where replaying a graph pays ("Distributed training", "Overlap and
+graphs": one CUDA graph per GPU)."""
 import numpy as np
 import pytest
 import torch
 
 import inputs as I
+import oracle as O
 
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import gradient_reduction_zero_gb300.dpz as dpz
-    from gpu_util import DEV, down, same_bits, up
+    from gpu_util import DEV, check_step, down, same_bits, up
 
 
-def _state(w):
+def _inputs(w):
     g = I.arena_host(w)
     th, m, v = (I.state_host(w, k) for k in ("master", "m", "v"))
     wts = np.zeros((w.N, w.P), dtype=np.uint16 if w.wdtype == "bf16" else np.float32)
-    return [up(x) for x in (g, th, m, v, wts)]
+    return g, th, m, v, wts
 
 
 @pytest.mark.parametrize("clip,acc32", [(0.0, False), (1e-3, False), (1e-3, True)])
@@ -29,7 +31,8 @@ def test_zero1_step_graph_replay_matches_eager(N, C, clip, acc32):
     w = I.TINY.with_(N=N, P=N * C, gdtype="bf16", wdtype="bf16", grad=I.Dist(I.NORMAL_TAIL, 1e-3),
                      m=I.Dist(I.NORMAL, 1e-4), v=I.Dist(I.ABS_NORMAL, 1e-6), step=7, clip=clip)
     cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)
-    eager = _state(w)
+    host = _inputs(w)
+    eager = [up(x) for x in host]
     graph = [t.clone() for t in eager]
     ws_e, ws_g = dpz.workspace(w.P, N, DEV), dpz.workspace(w.P, N, DEV)
     n_e = torch.zeros(1, device=DEV)
@@ -43,8 +46,18 @@ def test_zero1_step_graph_replay_matches_eager(N, C, clip, acc32):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=side):
         dpz.dp_zero1_step(*graph, N, cfg, ws=ws_g, norm_out=n_g, acc32=acc32)
-    # capture records the kernels without running them
-    for _ in range(reps):
+    # capture records the kernels without running them: the first replay is
+    # the first step, the oracle's step on the same inputs
+    g.replay()
+    torch.cuda.synchronize()
+    first = [down(t) for t in graph] + [n_g.item()]
+    first[0] = first[0].reshape(N, w.P)
+    first[4] = first[4].reshape(N, w.P)
+    check_step(w, *host, tuple(first), check_avg=clip > 0, acc32=acc32)
+    if clip <= 0:
+        assert same_bits(first[0], host[0])       # no averages stored without clip
+    assert dpz.ws_status(ws_g) == 0
+    for _ in range(reps - 1):
         g.replay()
     torch.cuda.synchronize()
     for a, b in zip(eager, graph):
@@ -66,3 +79,6 @@ def test_allreduce_graph_replay_matches_eager():
     graph.replay()
     torch.cuda.synchronize()
     assert same_bits(down(A), down(B))
+    ref = g0.copy()
+    O.ring_allreduce_avg(ref)
+    assert same_bits(down(B), ref)

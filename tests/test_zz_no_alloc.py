@@ -4,10 +4,12 @@ allocator owns the GPU, or a service that reserves its whole memory budget up
 front).  It keeps its partial sums in a fixed 4 MiB device array that the
 library declares, instead of a caller workspace.
 
-The GPU test calls it through the C-ABI twice in a row, on two different
-arenas, and compares each result with the workspace-based
-dp_grad_global_norm within the norm tolerance of the other tests (relative
-1e-6): a second call must not see anything the first one left behind."""
+The GPU test calls it through the C-ABI on arenas of different sizes and
+seeds, two calls in a row in both orders (large then small, and small then
+large, so that a slot or a first-stage sum left by a larger call would show),
+and requires each result to equal, bit for bit, the workspace-based
+dp_grad_global_norm (the same partials summed in the same fixed order), and
+the oracle's norm within the relative 1e-6 of the other norm tests."""
 import ctypes
 
 import numpy as np
@@ -37,8 +39,15 @@ def test_static_norm_rejects_arenas_beyond_its_scratch():
     assert rc == dpz.ERR_INVALID_ARG
 
 
+def _oracle_norm(w):
+    import oracle as O
+    from oracle_windows import oracle_full_sumsq
+    return O.clip_scale(oracle_full_sumsq(w), 0.0)[0]
+
+
 @pytest.mark.gpu
-def test_static_norm_matches_workspace_norm_twice():
+@pytest.mark.parametrize("order", ["large-then-small", "small-then-large"])
+def test_static_norm_matches_workspace_norm_twice(order):
     dpz = _lib()
     dev = torch.device("cuda:0")
     lib = ctypes.CDLL(dpz.LIB_PATH)
@@ -47,10 +56,14 @@ def test_static_norm_matches_workspace_norm_twice():
                    ctypes.c_void_p, ctypes.c_void_p]
     fn.restype = ctypes.c_int
     stream = torch.cuda.current_stream()
-    cases = [(8, 124_439_808 // 8, "bf16", 1e-3),    # the GPT-2 124M arena, near the limit
-             (3, 6152, "f32", 1.0)]                   # then a small one
-    for N, C, gdt, sigma in cases:
-        w = I.TINY.with_(N=N, P=N * C, gdtype=gdt, grad=I.Dist(I.NORMAL, sigma), grad_seed=N)
+    # (N, C, gradient dtype, sigma, seed): the GPT-2 124M arena at N = 8, near
+    # the scratch's limit, and a small fp32 arena at N = 3
+    large = (8, 124_439_808 // 8, "bf16", 1e-3, 8)
+    small = (3, 6152, "f32", 1.0, 3)
+    cases = [large, small] if order == "large-then-small" else \
+        [(3, 6152, "f32", 1.0, 31), (8, 124_439_808 // 8, "bf16", 1e-3, 81)]
+    for N, C, gdt, sigma, seed in cases:
+        w = I.TINY.with_(N=N, P=N * C, gdtype=gdt, grad=I.Dist(I.NORMAL, sigma), grad_seed=seed)
         G = torch.empty(w.N * w.P, dtype=torch.bfloat16 if gdt == "bf16" else torch.float32,
                         device=dev)
         I.fill_grads_device(w, G)
@@ -64,7 +77,10 @@ def test_static_norm_matches_workspace_norm_twice():
         assert rc == 0, dpz.lib.dpz_last_error()
         torch.cuda.synchronize()
         r, o = ref.item(), out.item()
-        assert r > 0 and abs(o - r) <= 1e-6 * r, (N, C, gdt, o, r)
+        assert np.float32(o).tobytes() == np.float32(r).tobytes(), (N, C, gdt, o, r)
+        onorm = _oracle_norm(w)
+        assert abs(o - onorm) <= 1e-6 * onorm, (N, C, gdt, o, onorm)
+        assert dpz.ws_status(ws) == 0
         del G, ws
     torch.cuda.empty_cache()
-    assert np.isfinite(o)
+    assert dpz.device_status() == 0
