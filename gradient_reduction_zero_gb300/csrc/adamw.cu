@@ -213,7 +213,7 @@ template <int GDT, int WDT>
 static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                             bool bcast, bool store_avg, void* grads, float* master, float* m,
                             float* v, void* weights, void* ws, cudaStream_t s,
-                            int64_t avg_stride, float* norm_out, bool early)
+                            int64_t avg_stride, float* norm_out)
 {
     if (src == AdamSrc::kFold) {
         if (zero1_fused_staged(a))   // staged through shared memory by bulk copies (staged.cu)
@@ -227,7 +227,7 @@ static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, A
     }
     if (bcast)      // staged through shared memory by bulk copies (staged.cu)
         return launch_adamw_bcast_tma(a, h, grads, avg_stride, master, m, v, weights, ws,
-                                      norm_out, early, s);
+                                      norm_out, s);
     return adamw_t<GDT, WDT, 0, false, false, false>(a, avg, h, false, grads, master, m, v,
                                                     weights, ws, s, avg_stride);
 }
@@ -277,7 +277,7 @@ cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h
 cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                          bool bcast, bool store_avg, void* grads, float* master, float* m,
                          float* v, void* weights, void* ws, cudaStream_t s, int64_t avg_stride,
-                         float* norm_out, bool early)
+                         float* norm_out)
 {
     if (a.gdt == 2) {
         // fp32-accumulating bf16 ring: only the fold differs; stored averages
@@ -285,26 +285,26 @@ cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, Adam
         if (src == AdamSrc::kFold) {
             if (a.wdt == 1)
                 return adamw_dt<2, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                                      weights, ws, s, avg_stride, norm_out, early);
+                                      weights, ws, s, avg_stride, norm_out);
             return adamw_dt<2, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                                  weights, ws, s, avg_stride, norm_out, early);
+                                  weights, ws, s, avg_stride, norm_out);
         }
         Arena b = a;
         b.gdt = 1;
         return launch_adamw(b, avg, h, src, bcast, store_avg, grads, master, m, v, weights, ws, s,
-                            avg_stride, norm_out, early);
+                            avg_stride, norm_out);
     }
     if (a.gdt == 1 && a.wdt == 1)
         return adamw_dt<1, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                              weights, ws, s, avg_stride, norm_out, early);
+                              weights, ws, s, avg_stride, norm_out);
     if (a.gdt == 1 && a.wdt == 0)
         return adamw_dt<1, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                              weights, ws, s, avg_stride, norm_out, early);
+                              weights, ws, s, avg_stride, norm_out);
     if (a.gdt == 0 && a.wdt == 1)
         return adamw_dt<0, 1>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                              weights, ws, s, avg_stride, norm_out, early);
+                              weights, ws, s, avg_stride, norm_out);
     return adamw_dt<0, 0>(a, avg, h, src, bcast, store_avg, grads, master, m, v,
-                          weights, ws, s, avg_stride, norm_out, early);
+                          weights, ws, s, avg_stride, norm_out);
 }
 
 }  // namespace dpz

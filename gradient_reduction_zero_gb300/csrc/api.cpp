@@ -374,12 +374,9 @@ DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v, void* 
         // cast + all-gather reading the stored averages
         DPZ_TRY(launch(s, [&] { return launch_reduce(a, avg, grads, false, ws, s); }));
         DPZ_TRY(launch(s, [&] { return launch_norm_finalize(a, ws, norm_out, s); }));
-        // launched early behind the finalisation: every kernel before it in
-        // the step was launched behind all earlier work on the stream, so its
-        // master/m/v loads may start before the finalisation ends
         DPZ_TRY(launch(s, [&] {
             return launch_adamw(a, avg, h, AdamSrc::kLoadOwner, true, false, grads, master, m, v,
-                                weights, ws, s, P, norm_out, true);
+                                weights, ws, s, P, norm_out);
         }));
     } else if (norm_out && zero1_fits_one_block(a)) {
         // a small arena: the step and its norm in one single-block launch

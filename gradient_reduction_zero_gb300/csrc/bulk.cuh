@@ -68,16 +68,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, long long limit
     return true;
 }
 
-// Programmatic dependent launch.  launch_dependents lets the next kernel on
-// the stream, if it was launched with programmatic stream serialisation,
-// begin before this one has finished; that kernel's wait_prior then blocks
-// until every earlier kernel has completed and its writes are visible.  In a
-// kernel launched the ordinary way, wait_prior returns at once.
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may begin once the blocks of the kernel before it on the
+// stream have exited, before that kernel's writes are flushed; wait_prior
+// blocks until every earlier kernel has completed and its writes are visible.
+// In a kernel launched the ordinary way it returns at once.
 __device__ __forceinline__ void pdl_wait_prior()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");

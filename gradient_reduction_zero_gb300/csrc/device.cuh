@@ -356,6 +356,37 @@ __device__ __forceinline__ float warp_sum_f32(float v)
     return v;
 }
 
+// warp_sum_f32 of eight values at once: v[s] is this lane's term of segment
+// s, and lane 4s receives segment s's sum.  Each level of the tree pairs the
+// same two lanes' values as warp_sum_f32 does, so every segment's sum has the
+// same bits; but at each level a lane hands half of its segments to its
+// partner and keeps the other half, so the eight trees take 4 + 2 + 1 + 1 + 1
+// = 9 shuffles instead of 40.
+__device__ __forceinline__ float warp_sum8_f32(const float v[8])
+{
+    const int lane = threadIdx.x & 31;
+    const bool hi16 = lane & 16, hi8 = lane & 8, hi4 = lane & 4;
+    float w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {           // lanes l, l^16: segments 0-3 stay below, 4-7 above
+        const float keep = hi16 ? v[4 + k] : v[k];
+        const float give = hi16 ? v[k] : v[4 + k];
+        w[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, give, 16));
+    }
+    float x[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {           // lanes l, l^8: halves of those four
+        const float keep = hi8 ? w[2 + k] : w[k];
+        const float give = hi8 ? w[k] : w[2 + k];
+        x[k] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, give, 8));
+    }
+    const float keep = hi4 ? x[1] : x[0];   // lanes l, l^4: one segment each
+    const float give = hi4 ? x[0] : x[1];
+    float y = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, give, 4));
+    y = __fadd_rn(y, __shfl_xor_sync(0xffffffffu, y, 2));
+    return __fadd_rn(y, __shfl_xor_sync(0xffffffffu, y, 1));
+}
+
 // Sum over the 32 lanes of a warp in a fixed tree; lane 0 holds the result.
 __device__ __forceinline__ double warp_sum(double v)
 {

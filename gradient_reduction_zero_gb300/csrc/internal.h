@@ -43,6 +43,10 @@ static_assert(offsetof(WsHeader, status) == DPZ_WS_STATUS_OFFSET,
 // finalisation turns them into a NaN norm and status bits.
 constexpr double kPartialNormSkipped = -1.0;   // the tile was not read
 constexpr double kPartialStepSkipped = -2.0;   // nor was its update written
+// Their high 32-bit words (the low words are 0); no sum of squares, not even a
+// NaN one, has either as its high word.
+constexpr int kPartialNormSkippedHi = (int)0xBFF00000u;
+constexpr int kPartialStepSkippedHi = (int)0xC0000000u;
 
 DPZ_HD inline int64_t segments_per_chunk(int64_t C) { return (C + kSegment - 1) / kSegment; }
 
@@ -109,21 +113,16 @@ struct RangeArgs {
 };
 cudaError_t launch_reduce_range(const Arena& a, const Avg& avg, const RangeArgs& g, void* ws,
                                 cudaStream_t s);
-// The finalisation is launched with programmatic stream serialisation: it
-// may start while the kernel before it drains, and waits for that kernel's
-// writes before it reads any partial.
+// The finalisation is launched with programmatic stream serialisation: its
+// blocks are placed while the kernel before it retires, and wait for that
+// kernel's writes before they read any partial.
 cudaError_t launch_norm_finalize(const Arena& a, void* ws, float* norm_out, cudaStream_t s);
 // norm_out: where the step's norm went (the bulk-copy staged update writes
-// NaN there if it gives up on a tile; may be NULL).  early: the staged update
-// may begin while the previous kernel on the stream finishes, issuing its
-// master/m/v loads before it waits for that kernel (programmatic dependent
-// launch).  Only for a kernel whose earlier work on the stream was launched
-// the ordinary way behind everything that writes master/m/v, as in
-// dp_zero1_step.
+// NaN there if it gives up on a tile; may be NULL).
 cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,
                          bool bcast, bool store_avg, void* grads, float* master, float* m,
                          float* v, void* weights, void* ws, cudaStream_t s,
-                         int64_t avg_stride, float* norm_out = nullptr, bool early = false);
+                         int64_t avg_stride, float* norm_out = nullptr);
 cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 
 // The whole step without clip, norm included, in one single-block launch, for
@@ -142,8 +141,7 @@ cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h
 // read_and_clear_pipeline_error returns.
 cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
                                    int64_t avg_stride, float* master, float* m, float* v,
-                                   void* weights, void* ws, float* norm_out, bool early,
-                                   cudaStream_t s);
+                                   void* weights, void* ws, float* norm_out, cudaStream_t s);
 // The step without clip, staged the same way (compile-time fold for N <= 8,
 // run-time fold beyond) where zero1_fused_staged holds: N <= 8, or N slab
 // tiles that fit shared memory with enough of them resident per SM to keep
@@ -179,11 +177,11 @@ cudaError_t static_scratch_address(void** ptr, cudaStream_t s);
 
 #if defined(__CUDACC__)
 // Launch `kernel` on `s` through cudaLaunchKernelEx.  early: with
-// programmatic stream serialisation, so that the kernel may begin once every
-// block of the previous kernel on the stream has begun (and executed
-// griddepcontrol.launch_dependents) instead of once it has finished; the
-// kernel must then execute griddepcontrol.wait before it touches anything
-// that earlier work writes or reads.
+// programmatic stream serialisation, so that the kernel may begin once the
+// blocks of the previous kernel on the stream have exited, before that
+// kernel's writes are flushed; the kernel must then execute
+// griddepcontrol.wait before it touches anything that earlier work writes or
+// reads.
 template <class... KArgs, class... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                                  cudaStream_t s, bool early, Args... args)

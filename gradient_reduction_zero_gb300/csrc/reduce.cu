@@ -148,7 +148,6 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
     const int64_t groups = C / kGroup;
     const int64_t segs = segments_per_chunk(C);
     const int lane = threadIdx.x & 31;
-    if (SUMSQ) pdl_launch_dependents();       // the norm finalisation may launch (it waits)
     if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     if constexpr (ReduceSegsPerWarp<GDT, NT, ALL>::value > 1) {
         reduce_segments<GDT, NT, ALL, SUMSQ, ReduceSegsPerWarp<GDT, NT, ALL>::value>(
@@ -221,7 +220,6 @@ k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restric
     const int64_t segs = segments_per_chunk(C);
     const int lane = threadIdx.x & 31;
     const int64_t sslab = src_stride * ES;
-    if (SUMSQ) pdl_launch_dependents();       // the norm finalisation may launch (it waits)
     if (SUMSQ && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     const int c = c_first + (int)blockIdx.y;
     const int64_t plo = lo > c * C ? lo : c * C;
@@ -269,11 +267,15 @@ struct StreamSegs {
 
 // Status bits a partial (or a first-stage sum) stands for: none for a sum of
 // squares, which is never negative; DPZ_STATUS_NORM_SKIPPED for
-// kPartialNormSkipped; both bits for kPartialStepSkipped.
+// kPartialNormSkipped (-1.0); both bits for kPartialStepSkipped (-2.0).  The
+// test compares the high words as integers: GB300's FP64 pipe is narrow, and
+// two FP64 compares per partial doubled the finalisation's time.
 __device__ __forceinline__ unsigned marker_bits(double x)
 {
-    return (x < 0.0 ? DPZ_STATUS_NORM_SKIPPED : 0u) |
-           (x < 0.5 * (kPartialNormSkipped + kPartialStepSkipped) ? DPZ_STATUS_UPDATE_SKIPPED : 0u);
+    const int hi = __double2hiint(x);
+    return hi == kPartialNormSkippedHi ? DPZ_STATUS_NORM_SKIPPED
+           : hi == kPartialStepSkippedHi ? DPZ_STATUS_NORM_SKIPPED | DPZ_STATUS_UPDATE_SKIPPED
+                                         : 0u;
 }
 
 // The block-wide OR of the threads' status bits (contains __syncthreads()).
@@ -295,14 +297,13 @@ __device__ __forceinline__ unsigned block_or_bits(unsigned b)
 // eight terms.  A partial that is a skipped tile's marker makes the norm NaN
 // and sets the status bits the marker stands for.
 //
-// The kernel is launched early behind the kernel that writes the partials
-// (programmatic dependent launch): it lets the update that follows launch
-// early in turn, then waits for the partials.
+// The kernel is launched early (programmatic dependent launch): its blocks
+// are placed while the kernel that writes the partials retires, and wait for
+// that kernel's writes before they read anything.
 __global__ void __launch_bounds__(kFinalThreads)
 k_norm_finalize(WsHeader* __restrict__ hdr, double* __restrict__ stage1,
                 const double* __restrict__ partials, int64_t n, float* __restrict__ norm_out)
 {
-    pdl_launch_dependents();
     pdl_wait_prior();
     const int F = gridDim.x;
     const int64_t L = (n + F - 1) / F;

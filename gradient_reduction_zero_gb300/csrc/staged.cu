@@ -14,10 +14,10 @@
 //   same load / update / store shape.  N up to 8 is compiled in; larger N
 //   fold at run time, on 1024- or 512-element tiles (64 threads), where
 //   enough of their tiles stay resident per SM (zero1_fused_tile).
-// - Sums of squares of the owner chunks (the standalone norm): one 32 KB tile
-//   per 256-thread CTA, one bulk load, then each warp takes segments of the
-//   tile.  Large tiles keep ~220 KB of loads in flight per SM; with 64 KB this
-//   kernel ran at 67 % of the copy peak, with 224 KB at 100 %.
+// - Sums of squares of the owner chunks (the standalone norm): one tile of
+//   4,096 elements per 64-thread CTA, one bulk load, then each warp takes eight
+//   segments of the tile at once.  Small tiles keep ~200 KB of loads in flight
+//   per SM (25 resident CTAs) and turn over quickly.
 //
 // Every wait on an mbarrier is bounded by the SM clock: if a tile has not
 // arrived after about two seconds the CTA sets the device error flag that
@@ -26,11 +26,6 @@
 // NaN norm and status bits; the update sets DPZ_STATUS_UPDATE_SKIPPED and a
 // NaN norm_out), waits (again bounded) for its loads in flight, and returns
 // without writing the tile.
-//
-// Kernel boundaries of the clipped step: the reduce kernel and the norm
-// finalisation let the next kernel launch early (griddepcontrol), and the
-// update issues its master/m/v loads before it waits for the finalisation, so
-// the first wave of the update streams while the finalisation runs.
 #include <atomic>
 
 #include "bulk.cuh"
@@ -68,11 +63,7 @@ struct TmaTile {
 // status word, where a skipped tile is reported; may be NULL without clip);
 // norm_out: set to NaN if this kernel gives up on a tile (may be NULL).
 // NT > 0: N == NT known at compile time; NT == 0: any N, read from n_rt.
-// master/m/v are requested before griddepcontrol.wait, the averages and the
-// norm after it: launched early behind the finalisation (dp_zero1_step), the
-// kernel's first wave loads its state while the finalisation runs.
-// Ten CTAs per SM (at most 48 registers a thread), as many as the kernel
-// held before its early-launch prologue was added.
+// Ten CTAs per SM (at most 48 registers a thread).
 template <int GDT, int WDT, int NT>
 __global__ void __launch_bounds__(kTmaThreads, 10)
 k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __restrict__ master,
@@ -103,13 +94,11 @@ k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __r
         mbar_init_one(&full);
         timed_out = 0;
         mbar_expect_tx(&full, (uint32_t)n * (GES + 12u) + wait.extra_tx);
+        bulk_load(t.avg, grads + ((int64_t)c * avg_stride + e) * GES, (uint32_t)n * GES, &full);
         bulk_load(t.th, master + e, (uint32_t)n * 4u, &full);
         bulk_load(t.m, mom + e, (uint32_t)n * 4u, &full);
         bulk_load(t.v, var + e, (uint32_t)n * 4u, &full);
     }
-    pdl_wait_prior();    // the averages and the norm are complete and visible
-    if (tid == 0)
-        bulk_load(t.avg, grads + ((int64_t)c * avg_stride + e) * GES, (uint32_t)n * GES, &full);
     __syncthreads();     // the barrier is initialised before anyone waits on it
 
     float scale = 1.0f;
@@ -207,7 +196,6 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
                   int n_rt, Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
                   double* __restrict__ partials, WaitSpec wait)
 {
-    pdl_launch_dependents();     // the norm finalisation may launch (it waits)
     using GS = Group<GDT>;
     using WS = Group<WDT>;
     constexpr int GES = GS::kBytes;
@@ -329,21 +317,32 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
 
 // ------------------------------------------------------------ norm
 
-constexpr int kNormTileBytes = 32768;
-constexpr int kNormThreads = 256;
+// Two warps per CTA, each taking eight consecutive 256-element segments of
+// the CTA's tile: 4,096 elements (8 KB of bf16, 16 KB of fp32).
+constexpr int kNormWarps = 2;
+constexpr int kNormThreads = 32 * kNormWarps;
+constexpr int kNormTile = 8 * kSegment * kNormWarps;
 
 // Sums of squares of the owner chunks (chunk c of slab c), one per 256-element
-// segment, from one kNormTileBytes tile per CTA.  The partial of a segment is
-// the same fixed shuffle tree over the same values as in every other kernel
-// that writes partials.
+// segment, from one kNormTile-element tile per CTA loaded by one bulk copy.
+// The partial of a segment is the same fixed shuffle tree over the same
+// values as in every other kernel that writes partials: a warp holds the
+// terms of its eight segments at once and adds them with warp_sum8_f32, whose
+// nine shuffles replace eight trees of five.  With the one tree per warp at a
+// time the kernel read the 1.5B arena's owner chunks at 6.78 TB/s; with the
+// eight trees interleaved 7.08, and with warp_sum8_f32 7.11 TB/s, against
+// 7.47 for the same bulk copies with no arithmetic.  Tiles of 4 to 32 KB ran
+// within 0.2 % of each other there; the small tiles were faster on small
+// arenas (the GPT-2 124M one: 5.46, 5.95 and 5.97 TB/s for 32 KB tiles with
+// one tree at a time, 32 KB and 8 KB tiles with warp_sum8_f32).
 template <int GDT>
 __global__ void __launch_bounds__(kNormThreads)
 k_norm_owned_tma(const char* __restrict__ grads, int64_t P, int64_t C,
                  WsHeader* __restrict__ hdr, double* __restrict__ partials, WaitSpec wait)
 {
-    pdl_launch_dependents();     // the norm finalisation may launch (it waits)
-    constexpr int ES = Group<GDT>::kBytes;
-    constexpr int T = kNormTileBytes / ES;            // elements per tile, a multiple of 256
+    using G = Group<GDT>;
+    constexpr int ES = G::kBytes;
+    constexpr int T = kNormTile;
     extern __shared__ __align__(128) unsigned char dsmem[];
     __shared__ __align__(8) uint64_t full;
     __shared__ int timed_out;
@@ -354,7 +353,8 @@ k_norm_owned_tma(const char* __restrict__ grads, int64_t P, int64_t C,
     const int64_t e = (int64_t)c * C + tc * T;
     const int64_t left = C - tc * T;
     const int n = (int)(left < T ? left : T);           // a multiple of 8
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    double* const tile_parts = partials + c * segments_per_chunk(C) + tc * (T / kSegment);
 
     if (blockIdx.x == 0 && tid == 0) hdr->arrive = 0u;
     if (tid == 0) {
@@ -364,29 +364,30 @@ k_norm_owned_tma(const char* __restrict__ grads, int64_t P, int64_t C,
         bulk_load(dsmem, grads + ((int64_t)c * P + e) * ES, (uint32_t)n * ES, &full);
     }
     __syncthreads();
-    const int64_t segs = segments_per_chunk(C);
-    const int nseg = (n + kSegment - 1) / kSegment;
     if (!mbar_wait_bounded(&full, wait.limit)) atomicExch(&timed_out, 1);
     __syncthreads();
+    // lane 4u of warp w writes the partial of the tile's segment 8w + u
+    const int sg_out = warp * 8 + (lane >> 2);
+    const bool writes = (lane & 3) == 0 && sg_out * kSegment < n;
     if (timed_out) {
         // the tile's partials say that its terms of the norm are missing
-        for (int sg = tid >> 5; sg < nseg; sg += kNormThreads / 32)
-            if (lane == 0) partials[c * segs + tc * (T / kSegment) + sg] = kPartialNormSkipped;
+        if (writes) tile_parts[sg_out] = kPartialNormSkipped;
         if (tid == 0) abandon_tile(&full, wait.limit);
         return;
     }
-    for (int sg = tid >> 5; sg < nseg; sg += kNormThreads / 32) {      // whole warps
-        const int i0 = sg * kSegment + lane * kGroup;
-        float ss = 0.0f;
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int i0 = (warp * 8 + u) * kSegment + lane * kGroup;
+        v[u] = 0.0f;
         if (i0 < n) {
             float x[8];
-            Group<GDT>::unpack(
-                *reinterpret_cast<const typename Group<GDT>::Raw*>(dsmem + (int64_t)i0 * ES), x);
-            ss = sumsq8(x);
+            G::unpack(*reinterpret_cast<const typename G::Raw*>(dsmem + (int64_t)i0 * ES), x);
+            v[u] = sumsq8(x);
         }
-        const float t = warp_sum_f32(ss);
-        if (lane == 0) partials[c * segs + tc * (T / kSegment) + sg] = (double)t;
     }
+    const float t = warp_sum8_f32(v);
+    if (writes) tile_parts[sg_out] = (double)t;
 }
 
 namespace {
@@ -422,7 +423,6 @@ struct UpdateLaunch {
     void* weights;
     void* ws;
     float* norm_out;
-    bool early;
 };
 
 template <int GDT, int WDT, int NT>
@@ -435,10 +435,11 @@ cudaError_t tma_t(const Arena& a, const AdamArgs& h, const UpdateLaunch& u, cuda
     if (e != cudaSuccess) return e;
     const int64_t tiles = (a.C + kTmaTile - 1) / kTmaTile * a.N;
     set_last_kernel_name("dpz_adamw_bcast");
-    return launch_kernel(fn, dim3((unsigned)tiles), dim3(kTmaThreads), smem, s, u.early,
-                         static_cast<const char*>(u.grads), u.avg_stride, u.master, u.m, u.v,
-                         static_cast<char*>(u.weights), a.P, a.C, a.N, h,
-                         static_cast<WsHeader*>(u.ws), u.norm_out, kWaitNormal);
+    fn<<<(unsigned)tiles, kTmaThreads, smem, s>>>(
+        static_cast<const char*>(u.grads), u.avg_stride, u.master, u.m, u.v,
+        static_cast<char*>(u.weights), a.P, a.C, a.N, h, static_cast<WsHeader*>(u.ws), u.norm_out,
+        kWaitNormal);
+    return cudaGetLastError();
 }
 
 template <int GDT, int WDT>
@@ -461,10 +462,9 @@ cudaError_t tma_n(const Arena& a, const AdamArgs& h, const UpdateLaunch& u, cuda
 
 cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
                                    int64_t avg_stride, float* master, float* m, float* v,
-                                   void* weights, void* ws, float* norm_out, bool early,
-                                   cudaStream_t s)
+                                   void* weights, void* ws, float* norm_out, cudaStream_t s)
 {
-    const UpdateLaunch u{grads, avg_stride, master, m, v, weights, ws, norm_out, early};
+    const UpdateLaunch u{grads, avg_stride, master, m, v, weights, ws, norm_out};
     const bool gbf = a.gdt != 0;       // stored averages: bf16 in both bf16 modes
     if (gbf && a.wdt == 1) return tma_n<1, 1>(a, h, u, s);
     if (gbf) return tma_n<1, 0>(a, h, u, s);
@@ -606,13 +606,10 @@ cudaError_t launch_zero1_fused_tma(const Arena& a, const Avg& avg, const AdamArg
 template <int GDT>
 static cudaError_t norm_t(const Arena& a, const void* grads, void* ws, cudaStream_t s)
 {
-    static SmemRaised raised;
     auto fn = k_norm_owned_tma<GDT>;
-    const cudaError_t e = allow_smem(raised, reinterpret_cast<const void*>(fn), kNormTileBytes);
-    if (e != cudaSuccess) return e;
-    constexpr int T = kNormTileBytes / Group<GDT>::kBytes;
-    const int64_t tiles = (a.C + T - 1) / T * a.N;
-    fn<<<(unsigned)tiles, kNormThreads, kNormTileBytes, s>>>(
+    constexpr size_t smem = (size_t)kNormTile * Group<GDT>::kBytes;   // at most 48 KB
+    const int64_t tiles = (a.C + kNormTile - 1) / kNormTile * a.N;
+    fn<<<(unsigned)tiles, kNormThreads, smem, s>>>(
         static_cast<const char*>(grads), a.P, a.C, static_cast<WsHeader*>(ws), ws_partials(ws),
         kWaitNormal);
     return cudaGetLastError();
@@ -673,11 +670,9 @@ cudaError_t launch_staged_timeout_selftest(int kernel, void* buf, cudaStream_t s
         return cudaGetLastError();
     }
     if (kernel == DPZ_SELFTEST_NORM) {
-        static SmemRaised raised;
         auto fn = k_norm_owned_tma<1>;
-        e = allow_smem(raised, reinterpret_cast<const void*>(fn), kNormTileBytes);
-        if (e != cudaSuccess) return e;
-        fn<<<1, kNormThreads, kNormTileBytes, s>>>(grads, a.P, a.C, hdr, ws_partials(ws), wait);
+        fn<<<1, kNormThreads, (size_t)kNormTile * 2, s>>>(grads, a.P, a.C, hdr, ws_partials(ws),
+                                                         wait);
     } else if (kernel == DPZ_SELFTEST_STEP) {
         static SmemRaised raised;
         auto fn = k_zero1_fused_tma<1, 1, 1, true, kTmaTile>;
