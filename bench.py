@@ -50,6 +50,7 @@ KERNEL_UNITS = {
     "dpz_rs_avg_sumsq": ("device.cuh", "internal.h", "reduce.cu"),
     "dpz_adamw_bcast": ("bulk.cuh", "device.cuh", "internal.h", "staged.cu"),
     "dpz_zero1_fused_sumsq": ("bulk.cuh", "device.cuh", "internal.h", "staged.cu"),
+    "dpz_norm_owned": ("bulk.cuh", "device.cuh", "internal.h", "staged.cu"),
 }
 
 
