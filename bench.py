@@ -586,6 +586,14 @@ def run_gpu(args) -> None:
         full = None if w.allreduce_only or w.clip <= 0 else (T, M, V, W, ws, cfg)
         e2e = run_e2e(args, w, G, step_with, nrm, stream, world, full)
 
+    # ------------------------------------------------ the other workloads
+    configs = None
+    if world == 1 and not args.no_configs and args.entry == "step" \
+            and args.workload == DEFAULT_WORKLOAD and args.clip is None:
+        del G, T, M, V, W
+        torch.cuda.empty_cache()
+        configs = measure_configs(args, dev, stream)
+
     cpu = cpu_mt = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = time_oracle(w, args.cpu_seconds)
@@ -625,12 +633,103 @@ def run_gpu(args) -> None:
             line["graph_replay"] = graph
         if prepared is not None:
             line["prepared_call"] = prepared
+        if configs is not None:
+            line["configs"] = configs
         if bucketed is not None:
             line["bucket_overlap"] = bucketed
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def time_median(fn, stream, steps: int) -> float:
+    """fn() `steps` times in min(steps, TIMING_REPS) groups of consecutive
+    calls, a CUDA event on `stream` before the first group and after each:
+    the median over the groups of the time per call, in ms."""
+    import torch
+    reps = min(steps, TIMING_REPS)
+    sizes = [steps // reps + (1 if g < steps % reps else 0) for g in range(reps)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for g, n in enumerate(sizes):
+        for _ in range(n):
+            fn()
+        ev[g + 1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(ev[g].elapsed_time(ev[g + 1]) / n for g, n in enumerate(sizes))
+
+
+def measure_configs(args, dev, stream) -> dict:
+    """The other workloads, timed on the device as the headline is (median
+    over groups of steps, after warm-up, inputs resident), each in its own
+    buffers, freed afterwards: the tiny step (also as 20 steps per CUDA
+    graph), the GPT-2 124M step, the GPT-2 1.5B step without clip, the 7B
+    all-reduce and the all-reduce sweep."""
+    import torch
+    import gradient_reduction_zero_gb300.dpz as dpz
+    peak = peaks()["hbm_gbs"]
+    rows = {}
+
+    def row(w, ms, extra=None):
+        b = step_bytes(w)
+        r = {"ms_per_step": round(ms, 5), "value": round(b / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+             "pct_of_measured_copy_peak": round(100 * b / (ms * 1e-3) / 1e9 / peak, 1),
+             "steps_per_s": round(1e3 / ms, 1), "l2": l2_note(w)}
+        if extra:
+            r.update(extra)
+        return r
+
+    def zero1(w, steps):
+        G, T, M, V, W = allocate(w, dev)
+        ws = dpz.workspace(w.P, w.N, dev)
+        nrm = torch.zeros(1, device=dev)
+        cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)
+
+        def step(on=stream):
+            dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=on)
+        for _ in range(max(3, args.warmup)):
+            step()
+        ms = time_median(step, stream, steps)
+        extra = {"clip": w.clip, "steps": steps}
+        if w.P * w.N < 1 << 20:
+            # launch-bound: the device time per step with 20 steps in one graph
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                on = torch.cuda.current_stream()
+                for _ in range(20):
+                    step(on)
+            for _ in range(3):
+                g.replay()
+            gms = time_median(g.replay, torch.cuda.current_stream(), 100) / 20
+            extra.update(graph_ms_per_step_20_per_graph=round(gms, 5),
+                         graph_steps_per_s=round(1e3 / gms, 1))
+        del G, T, M, V, W, ws
+        torch.cuda.empty_cache()
+        return row(w, ms, extra)
+
+    def allreduce(w, steps):
+        G, *_ = allocate(w, dev)
+        for _ in range(max(3, args.warmup)):
+            dpz.dp_allreduce_avg(G, w.N, stream)
+        ms = time_median(lambda: dpz.dp_allreduce_avg(G, w.N, stream), stream, steps)
+        del G
+        torch.cuda.empty_cache()
+        return row(w, ms, {"steps": steps})
+
+    rows[I.TINY.name] = zero1(I.TINY, 2000)
+    rows[I.GPT2_124M.name] = zero1(I.GPT2_124M, 50)
+    rows[I.GPT2_124M.name + " (no clip)"] = zero1(I.GPT2_124M.with_(clip=0.0), 50)
+    rows[I.GPT2_1P5B.name + " (no clip)"] = zero1(I.GPT2_1P5B.with_(clip=0.0), 20)
+    rows[I.ALLREDUCE_7B.name] = allreduce(I.ALLREDUCE_7B, 10)
+    for n in (2, 4, 8):
+        for size in I.SWEEP_SIZES:
+            w = I.allreduce_sweep(size, n)
+            rows[w.name] = allreduce(w, 200 if size < 1 << 26 else 20)
+    return rows
 
 
 def segment_bounds(P: int, N: int, k: int):
@@ -923,6 +1022,8 @@ def main(argv=None):
                     help="bf16 gradients reduced with fp32 accumulation (DPZ_BF16_ACC32)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads measured after the default one")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
     args = ap.parse_args(argv)
