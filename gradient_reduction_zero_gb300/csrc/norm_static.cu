@@ -6,8 +6,10 @@
 // the life of the process.  All calls share it and it keeps whatever the last
 // call wrote; the only field that must start at zero, the finalisation's
 // arrival counter, is cleared by the partial-sum kernel at the start of every
-// call.  Two calls whose kernels overlap on the GPU (different streams without
-// ordering between them) therefore race on the same scratch.
+// call, and every partial, first-stage sum and the status word are written
+// before they are read in the same call.  Two calls whose kernels overlap on
+// the GPU (different streams without ordering between them) therefore race
+// on the same scratch.
 #include <cuda_runtime.h>
 
 #include <atomic>

@@ -1,5 +1,5 @@
 // Kernels staged through shared memory by the Blackwell bulk-copy engine
-// (TMA, 1-D cp.async.bulk; bulk.cuh), both on one-shot, chunk-major grids:
+// (TMA, 1-D cp.async.bulk; bulk.cuh), all three on one-shot, chunk-major grids:
 //
 // - AdamW + cast + all-gather of the new weights from the stored averages:
 //   one 1024-element tile per 128-thread CTA.  Thread 0 issues the bulk loads

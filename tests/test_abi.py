@@ -206,3 +206,29 @@ def test_division_selftest_rejects_bad_args(dpz):
     assert dpz.lib.dpz_selftest_average_division(3, None, None) == 1    # NULL
     assert dpz.lib.dpz_selftest_average_division(3, A + 8, None) == 2   # misaligned
     assert b"mismatches" in dpz.lib.dpz_last_error()
+
+
+def test_prepared_call_validates_every_call(dpz):
+    """A prepared call makes the full C-ABI call each time, so the library's
+    argument checks run on every call: a chunk that is not a whole number of
+    8-element groups is refused before any launch (CPU tensors stand in for
+    device memory; nothing is launched)."""
+    import torch
+
+    class NoStream:
+        cuda_stream = 0
+
+    N, P = 4, 4 * 12                        # chunk of 12 elements: not a multiple of 8
+    G = torch.zeros(N * P)
+    T, M, V = torch.zeros(P), torch.zeros(P), torch.zeros(P)
+    W = torch.zeros(N * P, dtype=torch.bfloat16)
+    cfg = dpz.make_cfg(1e-3, 0.9, 0.999, 1e-8, 0.1, 1)
+    call = dpz.prepare_zero1_step(G, T, M, V, W, N, cfg, stream=NoStream())
+    for _ in range(2):
+        with pytest.raises(dpz.DpzError) as e:
+            call()
+        assert e.value.code == dpz.ERR_ALIGN
+        assert "multiple of 8" in str(e.value)
+    ar = dpz.prepare_allreduce_avg(G, N, stream=NoStream())
+    with pytest.raises(dpz.DpzError):
+        ar()

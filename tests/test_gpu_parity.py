@@ -129,6 +129,8 @@ def run_gpu_step(w, g, th, m, v, wts, store_avg=True, want_norm=True, fused=True
         dpz.zero1_adamw_step(G, T, M, V, W, w.N, cfg, ws=ws)
         dpz.dp_allgather(W, w.N)
     torch.cuda.synchronize()
+    if w.clip > 0 or want_norm:          # a finalisation ran: no tile was skipped
+        assert dpz.ws_status(ws) == 0
     return down(G), down(T), down(M), down(V), down(W), nrm.item()
 
 
