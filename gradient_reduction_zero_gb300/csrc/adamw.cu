@@ -129,48 +129,56 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
     }
 }
 
-// The whole step without clip for a small arena, norm included, in one block
-// of kFinalThreads (512) threads: each of the 16 warps takes segments w,
-// w + 16, ... of the list; then the block adds the segment partials exactly
-// as k_norm_finalize does when it runs as one block (lane t adds partials t,
-// t + 512, ... in order, then block_sum), and its second level only adds that
-// value to zeros (so warp 0's sum alone is taken).  So the norm has the same
-// bits as the two-kernel path, in one launch instead of two for arenas of at
-// most kSmallStepSegments segments, where launch latency is the cost.  The
-// fold is compiled for N (NT > 0, all N loads in flight at once) up to 8, and
-// warp 0 sums the partials from a shared-memory copy instead of reading back
-// the workspace.
-static_assert(kSmallStepSegments <= 32, "every partial is held by warp 0");
+// The whole step without clip for a small arena, norm included, in one
+// launch: a thread-block cluster of up to 8 CTAs (one per SM), each warp
+// taking one 256-element segment of the list.  Every warp writes its
+// segment's partial to the workspace and, over distributed shared memory,
+// into CTA 0's copy of sp.  After a cluster barrier, warp 0 of CTA 0 adds the
+// partials exactly as k_norm_finalize does when it runs as one block: thread t
+// holds 0 + partial t (t < total, else 0) and block_sum adds them with
+// warp_sum in each warp, then adds the warp sums with warp_sum again.  With
+// at most 32 partials every partial sits in warp 0, the other warps' sums are
+// +0, and adding +0 to a sum of squares leaves it unchanged, so warp 0's
+// warp_sum alone has the same bits.  So the norm is the two-kernel path's, in
+// one launch instead of two, for arenas of at most kSmallStepSegments
+// segments, where latency is the cost.  The fold is compiled for N (NT > 0,
+// all N loads in flight at once) up to 8.  Spreading the warps over a
+// cluster's SMs, instead of one 512-thread block on one SM, took the device
+// time per step (20 steps per CUDA graph) from 5.1 to 4.1 us for the tiny
+// arena (N = 4, 16 segments) and from 8.6-9.9 to 4.3-4.8 us at 32 segments;
+// a one-segment arena pays about 0.5 us for the cluster barriers (3.6 to 4.1).
+static_assert(kSmallStepSegments <= 32, "every partial is held by warp 0 of CTA 0");
+constexpr int kClusterCtas = 8;                      // portable cluster size
 
 template <int GDT, int WDT, int NT>
-__global__ void __launch_bounds__(kFinalThreads)
+__global__ void __launch_bounds__(32 * ((kSmallStepSegments + kClusterCtas - 1) / kClusterCtas))
 k_zero1_small(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
               float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int N,
               Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
               double* __restrict__ partials, float* __restrict__ norm_out)
 {
-    __shared__ double sp[kSmallStepSegments];
+    __shared__ double sp[kSmallStepSegments];       // CTA 0's copy receives the partials
     const int64_t segs = segments_per_chunk(C);
     const int64_t total = (int64_t)N * segs;        // <= kSmallStepSegments
     const int lane = threadIdx.x & 31;
-    for (int64_t sw = threadIdx.x >> 5; sw < total; sw += kFinalThreads / 32) {  // whole warps
+    const int64_t sw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    cluster_arrive_relaxed();      // CTA 0 has started before anyone writes its shared memory
+    float t = 0.0f;
+    if (sw < total) {                               // whole warps
         const SegPos p = seg_pos(sw, segs);
         const float ss = adamw_group<GDT, WDT, NT, true, true, true>(
             grads, master, mom, var, weights, P, C, N, p.c, p.seg * 32 + lane, avg, h,
             store_avg, false, 1.0f, P);
-        const float t = warp_sum_f32(ss);
-        if (lane == 0) {
-            partials[sw] = (double)t;                 // sw = p.c * segs + p.seg
-            sp[sw] = (double)t;
-        }
+        t = warp_sum_f32(ss);
     }
-    __syncthreads();     // every partial of the block is in shared memory
-    // k_norm_finalize as one block: thread t holds 0 + partial t (t < total,
-    // else 0), block_sum adds them with warp_sum in each warp and then adds the
-    // warp sums with warp_sum again.  With total <= 32 every partial sits in
-    // warp 0, the other warps' sums are +0, and adding +0 to a sum of squares
-    // leaves it unchanged, so warp 0's warp_sum alone has the same bits.
-    if (threadIdx.x >= 32) return;
+    cluster_wait();
+    if (sw < total && lane == 0) {
+        partials[sw] = (double)t;                   // sw = p.c * segs + p.seg
+        store_shared_of_rank(&sp[sw], 0, (double)t);
+    }
+    cluster_arrive_release();
+    cluster_wait();                                 // every partial is in CTA 0's sp
+    if (blockIdx.x != 0 || threadIdx.x >= 32) return;
     const double r = warp_sum(threadIdx.x < total ? 0.0 + sp[threadIdx.x] : 0.0);
     if (threadIdx.x == 0) {
         const float nrm = __double2float_rn(__dsqrt_rn(r));
@@ -237,41 +245,55 @@ bool zero1_fits_one_block(const Arena& a)
     return int64_t(a.N) * segments_per_chunk(a.C) <= kSmallStepSegments;
 }
 
+template <int GDT, int WDT, int NT>
+static cudaError_t small_t(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
+                           void* grads, float* master, float* m, float* v, void* weights,
+                           void* ws, float* norm_out, cudaStream_t s)
+{
+    const int64_t total = int64_t(a.N) * segments_per_chunk(a.C);
+    const unsigned warps = (unsigned)((total + kClusterCtas - 1) / kClusterCtas);   // per CTA
+    const unsigned ctas = (unsigned)((total + warps - 1) / warps);                  // <= 8
+    return launch_kernel(k_zero1_small<GDT, WDT, NT>, dim3(ctas), dim3(32 * warps), 0, s, false,
+                         ctas, static_cast<char*>(grads), master, m, v,
+                         static_cast<char*>(weights), a.P, a.C, a.N, avg, h, store_avg ? 1 : 0,
+                         static_cast<WsHeader*>(ws), ws_partials(ws), norm_out);
+}
+
+template <int GDT, int WDT>
+static cudaError_t small_n(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
+                           void* grads, float* master, float* m, float* v, void* weights,
+                           void* ws, float* norm_out, cudaStream_t s)
+{
+    switch (a.N) {
+    case 1: return small_t<GDT, WDT, 1>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    case 2: return small_t<GDT, WDT, 2>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    case 3: return small_t<GDT, WDT, 3>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    case 4: return small_t<GDT, WDT, 4>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    case 5: return small_t<GDT, WDT, 5>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    case 6: return small_t<GDT, WDT, 6>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    case 7: return small_t<GDT, WDT, 7>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    case 8: return small_t<GDT, WDT, 8>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    default: return small_t<GDT, WDT, 0>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    }
+}
+
 cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
                                void* grads, float* master, float* m, float* v, void* weights,
                                void* ws, float* norm_out, cudaStream_t s)
 {
     set_last_kernel_name("dpz_zero1_small");
-    char* g = static_cast<char*>(grads);
-    char* w = static_cast<char*>(weights);
-    WsHeader* hdr = static_cast<WsHeader*>(ws);
-    double* parts = ws_partials(ws);
-    const int sa = store_avg ? 1 : 0;
-#define DPZ_SMALL_N(GD, WD, NT)                                                              \
-    k_zero1_small<GD, WD, NT><<<1, kFinalThreads, 0, s>>>(g, master, m, v, w, a.P, a.C, a.N,  \
-                                                          avg, h, sa, hdr, parts, norm_out)
-#define DPZ_SMALL(GD, WD)                                                                      \
-    switch (a.N) {                                                                             \
-    case 1: DPZ_SMALL_N(GD, WD, 1); break;                                                     \
-    case 2: DPZ_SMALL_N(GD, WD, 2); break;                                                     \
-    case 3: DPZ_SMALL_N(GD, WD, 3); break;                                                     \
-    case 4: DPZ_SMALL_N(GD, WD, 4); break;                                                     \
-    case 5: DPZ_SMALL_N(GD, WD, 5); break;                                                     \
-    case 6: DPZ_SMALL_N(GD, WD, 6); break;                                                     \
-    case 7: DPZ_SMALL_N(GD, WD, 7); break;                                                     \
-    case 8: DPZ_SMALL_N(GD, WD, 8); break;                                                     \
-    default: DPZ_SMALL_N(GD, WD, 0); break;                                                    \
+    const bool wb = a.wdt == 1;
+    switch (a.gdt) {
+    case 0:
+        return wb ? small_n<0, 1>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s)
+                  : small_n<0, 0>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    case 1:
+        return wb ? small_n<1, 1>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s)
+                  : small_n<1, 0>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
+    default:
+        return wb ? small_n<2, 1>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s)
+                  : small_n<2, 0>(a, avg, h, store_avg, grads, master, m, v, weights, ws, norm_out, s);
     }
-    if (a.gdt == 2) {
-        if (a.wdt == 1) { DPZ_SMALL(2, 1); } else { DPZ_SMALL(2, 0); }
-    } else if (a.gdt == 1) {
-        if (a.wdt == 1) { DPZ_SMALL(1, 1); } else { DPZ_SMALL(1, 0); }
-    } else {
-        if (a.wdt == 1) { DPZ_SMALL(0, 1); } else { DPZ_SMALL(0, 0); }
-    }
-#undef DPZ_SMALL_N
-#undef DPZ_SMALL
-    return cudaGetLastError();
 }
 
 cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, AdamSrc src,

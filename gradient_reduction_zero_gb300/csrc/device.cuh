@@ -387,6 +387,41 @@ __device__ __forceinline__ float warp_sum8_f32(const float v[8])
     return __fadd_rn(y, __shfl_xor_sync(0xffffffffu, y, 1));
 }
 
+// ------------------------------------------------------------ clusters
+//
+// A thread-block cluster's CTAs run at the same time on different SMs and can
+// write each other's shared memory.  Every thread of every CTA of the cluster
+// must take part in each barrier.
+
+// Announce that this thread has started (no ordering of its memory accesses).
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// Announce that this thread's earlier memory accesses are done.
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+// Wait until every thread of the cluster has arrived; their released accesses
+// are then visible to this thread.
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store v into the copy of the shared-memory variable *p that the cluster's
+// CTA of the given rank holds.
+__device__ __forceinline__ void store_shared_of_rank(double* p, unsigned rank, double v)
+{
+    const uint32_t local = (uint32_t)__cvta_generic_to_shared(p);
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(remote), "d"(v) : "memory");
+}
+
 // Sum over the 32 lanes of a warp in a fixed tree; lane 0 holds the result.
 __device__ __forceinline__ double warp_sum(double v)
 {

@@ -125,9 +125,10 @@ cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, Adam
                          int64_t avg_stride, float* norm_out = nullptr);
 cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 
-// The whole step without clip, norm included, in one single-block launch, for
-// arenas of at most kSmallStepSegments 256-element segments (adamw.cu).  Same
-// results, bit for bit, as the fold kernel plus launch_norm_finalize.
+// The whole step without clip, norm included, in one launch of a thread-block
+// cluster (up to 8 CTAs, one warp per segment), for arenas of at most
+// kSmallStepSegments 256-element segments (adamw.cu).  Same results, bit for
+// bit, as the fold kernel plus launch_norm_finalize.
 constexpr int64_t kSmallStepSegments = 32;
 bool zero1_fits_one_block(const Arena& a);
 cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
@@ -182,20 +183,33 @@ cudaError_t static_scratch_address(void** ptr, cudaStream_t s);
 // kernel's writes are flushed; the kernel must then execute
 // griddepcontrol.wait before it touches anything that earlier work writes or
 // reads.
+// cluster > 0: the grid's CTAs form thread-block clusters of that many CTAs
+// along x (grid.x a multiple of it).
 template <class... KArgs, class... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                 cudaStream_t s, bool early, Args... args)
+                                 cudaStream_t s, bool early, unsigned cluster, Args... args)
 {
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (early) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 0) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cfg.attrs = early ? attr : nullptr;
-    cfg.numAttrs = early ? 1 : 0;
+    cfg.attrs = n > 0 ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 #endif

@@ -510,7 +510,7 @@ cudaError_t launch_norm_finalize(const Arena& a, void* ws, float* norm_out, cuda
     int64_t F = (n + 2047) / 2048;
     if (F > kFinalBlocks) F = kFinalBlocks;
     if (F < 1) F = 1;
-    return launch_kernel(k_norm_finalize, dim3((unsigned)F), dim3(kFinalThreads), 0, s, true,
+    return launch_kernel(k_norm_finalize, dim3((unsigned)F), dim3(kFinalThreads), 0, s, true, 0u,
                          static_cast<WsHeader*>(ws), ws_stage1(ws), ws_partials(ws), n, norm_out);
 }
 

@@ -208,7 +208,7 @@ DPZ_API int dp_allgather(void* weights, int64_t P, int N, int wdtype,
  * turn.  Without clipping it is one kernel that reads each gradient byte once
  * and writes the averages only if cfg->store_avg, plus the norm's
  * finalisation when norm_out is given (for arenas of at most 32 segments of
- * 256 elements, one single-block kernel does both); with clipping it is three
+ * 256 elements, one kernel on a thread-block cluster does both); with clipping it is three
  * (reduce + norm partials and averages store, norm finalize, AdamW + cast +
  * broadcast), because the clip scale depends on every element.  norm_out
  * (device, may be NULL) receives the global norm; ws is required when

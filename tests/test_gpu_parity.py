@@ -196,7 +196,7 @@ def test_fused_equals_unfused(N, C, clip):
 @pytest.mark.parametrize("gdt", ["f32", "bf16"])
 def test_small_step_is_one_launch_and_identical(N, C, launches, gdt):
     """Without clip and with the norm wanted, an arena of at most 32 segments
-    runs the step and its norm in one single-block launch; larger ones use the
+    runs the step and its norm in one launch (a thread-block cluster); larger ones use the
     fold kernel plus the finalisation.  Both give the four separate calls'
     bits, the norm included."""
     w, g, th, m, v, wts = make_problem(N, C, gdt, "bf16", 0.0, seed=C + N)
