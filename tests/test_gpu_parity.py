@@ -210,6 +210,50 @@ def test_small_step_is_one_launch_and_identical(N, C, launches, gdt):
     check_step(w, g, th, m, v, wts, a)
 
 
+@pytest.mark.parametrize("N,segs", [(1, 1), (1, 2), (1, 3), (1, 5), (1, 8), (1, 9), (1, 15),
+                                    (1, 17), (1, 24), (1, 25), (1, 31), (1, 32), (2, 7),
+                                    (3, 10), (4, 8), (5, 6), (7, 4), (8, 4), (16, 2), (32, 1)])
+def test_small_step_every_cluster_shape(N, segs):
+    """The one-launch small step spreads 1 to 32 segments over a thread-block
+    cluster of up to 8 CTAs (1 to 4 warps each; some warps of the last CTA
+    idle).  Every shape gives the four separate calls' bits, the norm
+    included, and the oracle's.  Each chunk ends in a ragged segment."""
+    C = segs * 256 - 8
+    w, g, th, m, v, wts = make_problem(N, C, "bf16", "bf16", 0.0, seed=N * 64 + segs)
+    before = dpz.launch_count()
+    a = run_gpu_step(w, g, th, m, v, wts, fused=True)
+    assert dpz.launch_count() - before == 1
+    b = run_gpu_step(w, g, th, m, v, wts, fused=False)
+    for x, y in zip(a[:5], b[:5]):
+        assert same_bits(x, y)
+    assert a[5] == b[5]
+    check_step(w, g, th, m, v, wts, a)
+
+
+def test_prepared_call_equals_plain_call():
+    """A prepared step (arguments marshalled once) gives the plain call's
+    bits, step after step."""
+    w, g, th, m, v, wts = make_problem(4, 6152, "bf16", "bf16", 1e-3, seed=77)
+    outs = []
+    for prepared in (False, True):
+        G, T, M, V, W = up(g), up(th), up(m), up(v), up(wts)
+        ws = dpz.workspace(w.P, w.N, DEV)
+        nrm = torch.zeros(1, device=DEV)
+        cfg = dpz.make_cfg(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.step, w.clip)
+        if prepared:
+            call = dpz.prepare_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm)
+            for _ in range(3):
+                call()
+        else:
+            for _ in range(3):
+                dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm)
+        torch.cuda.synchronize()
+        outs.append([down(x) for x in (G, T, M, V, W)] + [nrm.item()])
+    for x, y in zip(outs[0][:5], outs[1][:5]):
+        assert same_bits(x, y)
+    assert outs[0][5] == outs[1][5]
+
+
 @pytest.mark.parametrize("store_avg,want_norm", [(False, False), (False, True), (True, False)])
 def test_no_clip_variants(store_avg, want_norm):
     N, C = 4, 6152
