@@ -95,17 +95,20 @@ Range range(const char* name, const void* p, int64_t bytes)
 }
 
 // The byte ranges of one call's buffers, held on the stack (no allocation on
-// the launch path).  A NULL buffer is not added.
+// the launch path).  A NULL buffer is not added.  No call has more than seven
+// buffers; one past kMax would be dropped, never written out of bounds.
 struct Ranges {
-    Range r[8];
+    static constexpr int kMax = 8;
+    Range r[kMax];
     int n = 0;
     Ranges(std::initializer_list<Range> rs)
     {
-        for (const Range& x : rs) r[n++] = x;
+        for (const Range& x : rs)
+            if (n < kMax) r[n++] = x;
     }
     void add(const char* name, const void* p, int64_t bytes)
     {
-        if (p != nullptr) r[n++] = range(name, p, bytes);
+        if (p != nullptr && n < kMax) r[n++] = range(name, p, bytes);
     }
 };
 
