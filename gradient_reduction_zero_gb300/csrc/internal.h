@@ -172,7 +172,7 @@ cudaError_t launch_selftest_division(const Avg& avg, unsigned long long* mismatc
 
 // The fixed device scratch of dp_grad_global_norm_static (norm_static.cu):
 // its size in bytes, and its device address on the current device (looked up
-// on every call outside a stream capture on `s`, reused during one).
+// again on every call made outside a stream capture on `s`).
 size_t static_scratch_bytes();
 cudaError_t static_scratch_address(void** ptr, cudaStream_t s);
 

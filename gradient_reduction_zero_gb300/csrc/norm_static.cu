@@ -36,10 +36,10 @@ size_t static_scratch_bytes() { return kStaticScratchBytes; }
 // The array's device address on the current device.  In host code the name
 // g_norm_scratch is only a stand-in for the symbol, so the address comes from
 // cudaGetSymbolAddress, with the device current.  It is looked up again on
-// every call that is not being captured into a CUDA graph (a device reset
-// loads the module anew, and the array may then sit elsewhere), and taken
-// from the last such lookup during a capture, where the lookup itself may not
-// be allowed; a capture before any uncaptured call on the device fails.
+// every call made outside a stream capture (a device reset loads the module
+// anew, and the array may then sit elsewhere); while `s` is capturing, the
+// lookup is not made and the last one on the device is used, or the call
+// fails if there was none.
 cudaError_t static_scratch_address(void** ptr, cudaStream_t s)
 {
     int dev = 0;

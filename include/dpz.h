@@ -301,9 +301,8 @@ DPZ_API int dp_zero2_update(const void* shards, float* master, float* m, float* 
  *
  * The first call on a device looks up the array's address on that device
  * (cudaGetSymbolAddress), so make that first call before any stream capture.
- * Every later call that is not being captured looks it up again (after a
- * device reset the array may sit elsewhere); a call inside a capture reuses
- * the last lookup on its device and fails with DPZ_ERR_CUDA if there was none.
+ * Every later call made outside a stream capture looks it up again (after a
+ * device reset the array may sit elsewhere).
  * Every GPU that loads the library holds the 4 MiB array until the process
  * exits.  All calls share it: each call clears what must start at zero, but
  * calls whose kernels overlap on the GPU (unordered streams) race with each
