@@ -130,49 +130,190 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
 }
 
 // The whole step without clip for a small arena, norm included, in one
-// launch: a thread-block cluster of up to 8 CTAs (one per SM), each warp
-// taking one 256-element segment of the list.  Every warp writes its
-// segment's partial to the workspace and, over distributed shared memory,
-// into CTA 0's copy of sp.  After a cluster barrier, warp 0 of CTA 0 adds the
-// partials exactly as k_norm_finalize does when it runs as one block: thread t
-// holds 0 + partial t (t < total, else 0) and block_sum adds them with
-// warp_sum in each warp, then adds the warp sums with warp_sum again.  With
-// at most 32 partials every partial sits in warp 0, the other warps' sums are
-// +0, and adding +0 to a sum of squares leaves it unchanged, so warp 0's
-// warp_sum alone has the same bits.  So the norm is the two-kernel path's, in
-// one launch instead of two, for arenas of at most kSmallStepSegments
-// segments, where latency is the cost.  The fold is compiled for N (NT > 0,
-// all N loads in flight at once) up to 8.  Spreading the warps over a
-// cluster's SMs, instead of one 512-thread block on one SM, took the device
-// time per step (20 steps per CUDA graph) from 5.1 to 4.1 us for the tiny
-// arena (N = 4, 16 segments) and from 8.6-9.9 to 4.3-4.8 us at 32 segments;
-// a one-segment arena pays about 0.5 us for the cluster barriers (3.6 to 4.1).
+// launch: a thread-block cluster of up to 8 CTAs (one per SM).  Each
+// 256-element segment of the list gets a team of four warps, and each thread
+// two consecutive elements of one 8-element group (lanes 4k .. 4k+3 of a warp
+// share group k), so every thread's serial chain of loads, ring fold,
+// average, AdamW and stores covers 2 elements instead of 8.  The segment's
+// partial is the same fixed tree as everywhere else: each thread squares and
+// adds its pair (sumsq8's first level), the 4-lane shuffles add the pairs as
+// sumsq8's second and third levels do, and the first warp of the team adds the
+// 32 group sums with warp_sum_f32, group g in lane g.  Every team writes its
+// partial to the workspace and, over distributed shared memory, into CTA 0's
+// copy of sp.  After a cluster barrier, warp 0 of CTA 0 adds the partials
+// exactly as k_norm_finalize does when it runs as one block: thread t holds
+// 0 + partial t (t < total, else 0) and block_sum adds them with warp_sum in
+// each warp, then adds the warp sums with warp_sum again.  With at most 32
+// partials every partial sits in warp 0, the other warps' sums are +0, and
+// adding +0 to a sum of squares leaves it unchanged, so warp 0's warp_sum
+// alone has the same bits.  So the step and its norm equal the two-kernel
+// path's bit for bit, in one launch instead of two, for arenas of at most
+// kSmallStepSegments segments, where latency is the cost.  The average takes
+// the correctly rounded quotient element by element (Markstein's correction
+// where its theorem holds, else IEEE division), the same value divide8 gives.
+// Device time per step (20 steps per CUDA graph), tiny arena (N = 4, 16
+// segments): one 512-thread block 5.1 us, a cluster with one warp per
+// segment 3.9 us, four warps per segment 3.4 us (32 segments: 4.3-4.7 and
+// 3.7-4.1 us; one segment: 4.1 and 3.2 us).
 static_assert(kSmallStepSegments <= 32, "every partial is held by warp 0 of CTA 0");
-constexpr int kClusterCtas = 8;                      // portable cluster size
+constexpr int kClusterCtas = 8;                                 // portable cluster size
+constexpr int kTeam = 128;                                      // threads per segment
+constexpr int kSmallMaxThreads =
+    kTeam * (int)((kSmallStepSegments + kClusterCtas - 1) / kClusterCtas);
+
+// Two consecutive elements of one storage type, as Group does for eight.
+template <int DT>
+struct Pair;
+
+template <>
+struct Pair<0> {
+    static __device__ __forceinline__ void load(const char* p, float x[2])
+    {
+        const float2 v = *reinterpret_cast<const float2*>(p);
+        x[0] = v.x;
+        x[1] = v.y;
+    }
+    static __device__ __forceinline__ void store(char* p, const float x[2])
+    {
+        *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+    }
+    static __device__ __forceinline__ void round2(float[2]) {}
+    static __device__ __forceinline__ void hop_round2(float[2]) {}
+};
+
+template <>
+struct Pair<1> {
+    static __device__ __forceinline__ void load(const char* p, float x[2])
+    {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+        x[0] = bf16_lo(w);
+        x[1] = bf16_hi(w);
+    }
+    static __device__ __forceinline__ void store(char* p, const float x[2])
+    {
+        *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(x[0], x[1]);
+    }
+    static __device__ __forceinline__ void round2(float x[2]) { round_bf16x2(x[0], x[1]); }
+    static __device__ __forceinline__ void hop_round2(float x[2]) { round2(x); }
+};
+
+template <>
+struct Pair<2> : Pair<1> {
+    static __device__ __forceinline__ void hop_round2(float[2]) {}
+};
+
+// a / N correctly rounded, one element at a time: the value divide8 gives
+// (its two paths agree with IEEE division for every float, so which path an
+// element takes does not change its bits).
+template <int NT>
+__device__ __forceinline__ float divide1(float a, const Avg& avg)
+{
+    constexpr bool kPow2 = NT > 0 && (NT & (NT - 1)) == 0;
+    if (kPow2 || (NT == 0 && avg.pow2)) return __fmul_rn(a, avg.invN);
+    return markstein_ok(a) ? div_markstein(a, avg.fN, avg.invN) : __fdiv_rn(a, avg.fN);
+}
+
+// The work of one thread: elements e and e + 1 of chunk c (the step without
+// clip); returns their sum of squares, x0*x0 + x1*x1 (0 if nothing to do).
+template <int GDT, int WDT, int NT>
+__device__ __forceinline__ float small_pair(char* __restrict__ grads, float* __restrict__ master,
+                                            float* __restrict__ mom, float* __restrict__ var,
+                                            char* __restrict__ weights, int64_t P, int N, int c,
+                                            int64_t e, const Avg& avg, const AdamArgs& h,
+                                            int store_avg)
+{
+    using G = Pair<GDT>;
+    constexpr int GES = Group<GDT>::kBytes;
+    constexpr int WES = Group<WDT>::kBytes;
+    const int64_t gslab = P * GES;
+    float g[2];
+    if constexpr (NT > 0) {
+        float x[NT][2];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {                  // ring order: slabs c+1, ..., c
+            int r = c + 1 + j;
+            if (r >= NT) r -= NT;
+            G::load(grads + r * gslab + e * GES, x[j]);
+        }
+        g[0] = x[0][0];
+        g[1] = x[0][1];
+#pragma unroll
+        for (int j = 1; j < NT; ++j) {
+            g[0] = __fadd_rn(g[0], x[j][0]);
+            g[1] = __fadd_rn(g[1], x[j][1]);
+            G::hop_round2(g);
+        }
+    } else {
+        int r = c + 1;
+        if (r >= N) r -= N;
+        G::load(grads + r * gslab + e * GES, g);
+        for (int j = 2; j <= N; ++j) {
+            ++r;
+            if (r >= N) r -= N;
+            float x[2];
+            G::load(grads + r * gslab + e * GES, x);
+            g[0] = __fadd_rn(g[0], x[0]);
+            g[1] = __fadd_rn(g[1], x[1]);
+            G::hop_round2(g);
+        }
+    }
+    g[0] = divide1<NT>(g[0], avg);
+    g[1] = divide1<NT>(g[1], avg);
+    G::round2(g);
+    if (store_avg) G::store(grads + c * gslab + e * GES, g);
+    const float ss = __fadd_rn(__fmul_rn(g[0], g[0]), __fmul_rn(g[1], g[1]));
+    float th[2], mm[2], vv[2];
+    Pair<0>::load(reinterpret_cast<const char*>(master + e), th);
+    Pair<0>::load(reinterpret_cast<const char*>(mom + e), mm);
+    Pair<0>::load(reinterpret_cast<const char*>(var + e), vv);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) adamw_elem(th[q], mm[q], vv[q], g[q], h);
+    Pair<0>::store(reinterpret_cast<char*>(master + e), th);
+    Pair<0>::store(reinterpret_cast<char*>(mom + e), mm);
+    Pair<0>::store(reinterpret_cast<char*>(var + e), vv);
+    const int64_t wslab = P * WES;
+    if constexpr (NT > 0) {
+#pragma unroll
+        for (int r = 0; r < NT; ++r) Pair<WDT>::store(weights + r * wslab + e * WES, th);
+    } else {
+        for (int r = 0; r < N; ++r) Pair<WDT>::store(weights + r * wslab + e * WES, th);
+    }
+    return ss;
+}
 
 template <int GDT, int WDT, int NT>
-__global__ void __launch_bounds__(32 * ((kSmallStepSegments + kClusterCtas - 1) / kClusterCtas))
+__global__ void __launch_bounds__(kSmallMaxThreads)
 k_zero1_small(char* __restrict__ grads, float* __restrict__ master, float* __restrict__ mom,
               float* __restrict__ var, char* __restrict__ weights, int64_t P, int64_t C, int N,
               Avg avg, AdamArgs h, int store_avg, WsHeader* __restrict__ hdr,
               double* __restrict__ partials, float* __restrict__ norm_out)
 {
     __shared__ double sp[kSmallStepSegments];       // CTA 0's copy receives the partials
+    __shared__ float gsum[kSmallMaxThreads / kTeam][32];   // each team's 32 group sums
     const int64_t segs = segments_per_chunk(C);
     const int64_t total = (int64_t)N * segs;        // <= kSmallStepSegments
-    const int lane = threadIdx.x & 31;
-    const int64_t sw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int team = tid / kTeam, tt = tid % kTeam;
+    const int grp = tt >> 2, quarter = tt & 3;       // group of the segment, pair of the group
+    const int64_t sw = (int64_t)blockIdx.x * (blockDim.x / kTeam) + team;
     cluster_arrive_relaxed();      // CTA 0 has started before anyone writes its shared memory
-    float t = 0.0f;
-    if (sw < total) {                               // whole warps
+    float s = 0.0f;
+    if (sw < total) {                               // whole teams
         const SegPos p = seg_pos(sw, segs);
-        const float ss = adamw_group<GDT, WDT, NT, true, true, true>(
-            grads, master, mom, var, weights, P, C, N, p.c, p.seg * 32 + lane, avg, h,
-            store_avg, false, 1.0f, P);
-        t = warp_sum_f32(ss);
+        const int64_t gi = p.seg * 32 + grp;
+        if (gi < C / kGroup)
+            s = small_pair<GDT, WDT, NT>(grads, master, mom, var, weights, P, N, p.c,
+                                         p.c * C + gi * kGroup + 2 * quarter, avg, h, store_avg);
     }
+    // the group's sum of squares in sumsq8's tree: (p0 + p1) + (p2 + p3)
+    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 1));
+    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2));
+    if (quarter == 0) gsum[team][grp] = s;
+    __syncthreads();
+    float t = 0.0f;
+    if (tt < 32 && sw < total) t = warp_sum_f32(gsum[team][lane]);   // whole warps
     cluster_wait();
-    if (sw < total && lane == 0) {
+    if (sw < total && tt == 0) {
         partials[sw] = (double)t;                   // sw = p.c * segs + p.seg
         store_shared_of_rank(&sp[sw], 0, (double)t);
     }
@@ -251,9 +392,9 @@ static cudaError_t small_t(const Arena& a, const Avg& avg, const AdamArgs& h, bo
                            void* ws, float* norm_out, cudaStream_t s)
 {
     const int64_t total = int64_t(a.N) * segments_per_chunk(a.C);
-    const unsigned warps = (unsigned)((total + kClusterCtas - 1) / kClusterCtas);   // per CTA
-    const unsigned ctas = (unsigned)((total + warps - 1) / warps);                  // <= 8
-    return launch_kernel(k_zero1_small<GDT, WDT, NT>, dim3(ctas), dim3(32 * warps), 0, s, false,
+    const unsigned teams = (unsigned)((total + kClusterCtas - 1) / kClusterCtas);   // per CTA
+    const unsigned ctas = (unsigned)((total + teams - 1) / teams);                  // <= 8
+    return launch_kernel(k_zero1_small<GDT, WDT, NT>, dim3(ctas), dim3(kTeam * teams), 0, s, false,
                          ctas, static_cast<char*>(grads), master, m, v,
                          static_cast<char*>(weights), a.P, a.C, a.N, avg, h, store_avg ? 1 : 0,
                          static_cast<WsHeader*>(ws), ws_partials(ws), norm_out);

@@ -126,7 +126,7 @@ cudaError_t launch_adamw(const Arena& a, const Avg& avg, const AdamArgs& h, Adam
 cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 
 // The whole step without clip, norm included, in one launch of a thread-block
-// cluster (up to 8 CTAs, one warp per segment), for arenas of at most
+// cluster (up to 8 CTAs, four warps per segment), for arenas of at most
 // kSmallStepSegments 256-element segments (adamw.cu).  Same results, bit for
 // bit, as the fold kernel plus launch_norm_finalize.
 constexpr int64_t kSmallStepSegments = 32;
