@@ -381,7 +381,7 @@ static cudaError_t adamw_dt(const Arena& a, const Avg& avg, const AdamArgs& h, A
                                                     weights, ws, s, avg_stride);
 }
 
-bool zero1_fits_one_block(const Arena& a)
+bool zero1_fits_small_step(const Arena& a)
 {
     return int64_t(a.N) * segments_per_chunk(a.C) <= kSmallStepSegments;
 }

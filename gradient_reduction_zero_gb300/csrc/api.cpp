@@ -381,7 +381,7 @@ DPZ_API int dp_zero1_step(void* grads, float* master, float* m, float* v, void* 
             return launch_adamw(a, avg, h, AdamSrc::kLoadOwner, true, false, grads, master, m, v,
                                 weights, ws, s, P, norm_out);
         }));
-    } else if (norm_out && zero1_fits_one_block(a)) {
+    } else if (norm_out && zero1_fits_small_step(a)) {
         // a small arena: the step and its norm in one launch (a thread-block cluster)
         DPZ_TRY(launch(s, [&] {
             return launch_zero1_small(a, avg, h, cfg->store_avg != 0, grads, master, m, v,

@@ -1,6 +1,8 @@
-// Device helpers shared by the streaming kernels: 16-byte streaming loads and
-// stores, bf16 packing with round-to-nearest-even, the ring-order fold, the
-// fp32 AdamW element update and a deterministic block sum.
+// Device helpers shared by the streaming kernels: 16- and 32-byte streaming
+// loads and stores, bf16 packing with round-to-nearest-even, the ring-order
+// fold, the correctly rounded average, the fp32 AdamW element update, the
+// fixed warp and block sums (one segment's, or eight segments' at once), and
+// thread-block cluster barriers and stores into another CTA's shared memory.
 #pragma once
 
 #include <cuda_bf16.h>

@@ -130,7 +130,7 @@ cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s);
 // kSmallStepSegments 256-element segments (adamw.cu).  Same results, bit for
 // bit, as the fold kernel plus launch_norm_finalize.
 constexpr int64_t kSmallStepSegments = 32;
-bool zero1_fits_one_block(const Arena& a);
+bool zero1_fits_small_step(const Arena& a);
 cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h, bool store_avg,
                                void* grads, float* master, float* m, float* v, void* weights,
                                void* ws, float* norm_out, cudaStream_t s);
@@ -138,8 +138,9 @@ cudaError_t launch_zero1_small(const Arena& a, const Avg& avg, const AdamArgs& h
 // AdamW + cast + all-gather from the stored averages (element e of chunk c
 // at grads + c*avg_stride + e), staged through shared memory by bulk copies
 // (staged.cu, as is launch_norm_owned).  A tile that does not arrive within
-// the wait limit sets the device error flag that
-// read_and_clear_pipeline_error returns.
+// the wait limit is reported in the workspace's status word and as a NaN in
+// norm_out, and sets the device error flag that read_and_clear_pipeline_error
+// returns.
 cudaError_t launch_adamw_bcast_tma(const Arena& a, const AdamArgs& h, const void* grads,
                                    int64_t avg_stride, float* master, float* m, float* v,
                                    void* weights, void* ws, float* norm_out, cudaStream_t s);
@@ -155,8 +156,8 @@ cudaError_t launch_zero1_fused_tma(const Arena& a, const Avg& avg, const AdamArg
 cudaError_t read_and_clear_pipeline_error(unsigned* flag);
 // Launch one staged kernel (DPZ_SELFTEST_* of dpz.h) on the one-tile arena
 // laid out in `buf` (DPZ_SELFTEST_BUF_BYTES), with a barrier that never
-// completes and a short wait bound, so that its wait runs out; then the norm
-// finalisation where the kernel writes partials.
+// completes and a short wait bound, so that its wait runs out.  Where the
+// kernel writes partials, the caller then launches the norm finalisation.
 cudaError_t launch_staged_timeout_selftest(int kernel, void* buf, cudaStream_t s);
 // The self-test's arena (N = 1, P = 8, bf16 gradients and weights) and its
 // layout in the buffer: the workspace at 0, norm_out, then gradients, master,
