@@ -219,7 +219,7 @@ DPZ_API size_t dpz_workspace_bytes(int64_t P, int N)
 
 DPZ_API const char* dpz_last_error(void) { return g_err.c_str(); }
 
-DPZ_API const char* dpz_version(void) { return "dpz 0.1 (sm_103a)"; }
+DPZ_API const char* dpz_version(void) { return "dpz 0.2 (sm_103a)"; }
 
 DPZ_API int64_t dpz_launch_count(void) { return g_launches.load(); }
 
