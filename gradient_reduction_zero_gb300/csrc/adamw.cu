@@ -142,8 +142,9 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
 // partial to the workspace and, over distributed shared memory, into CTA 0's
 // copy of sp.  After a cluster barrier, warp 0 of CTA 0 adds the partials
 // exactly as k_norm_finalize does when it runs as one block: thread t holds
-// 0 + partial t (t < total, else 0) and block_sum adds them with warp_sum in
-// each warp, then adds the warp sums with warp_sum again.  With at most 32
+// partial t (t < total, else 0; a chain of one term gives its term back, by
+// Sum2 or in fp64) and block_sum adds them with warp_sum in each warp, then
+// adds the warp sums with warp_sum again.  With at most 32
 // partials every partial sits in warp 0, the other warps' sums are +0, and
 // adding +0 to a sum of squares leaves it unchanged, so warp 0's warp_sum
 // alone has the same bits.  So the step and its norm equal the two-kernel

@@ -287,18 +287,60 @@ __device__ __forceinline__ unsigned block_or_bits(unsigned b)
     return norm | upd;
 }
 
+// A partial as the fp32 value it holds.  Every partial is a 256-element sum of
+// squares computed in fp32 and stored as a double: +0, or a double whose low
+// 29 mantissa bits are zero and whose exponent lies in fp32's normal range.
+// The fp32 value is then rebuilt from the double's two words with integer
+// operations (a double-to-float conversion runs on the narrow FP64 pipe).  A
+// partial of any other form (an fp32 subnormal, inf, NaN, a skipped tile's
+// negative marker) leaves a trace in odd_low or odd_exp, and the caller then
+// adds that chain in fp64 instead.
+constexpr unsigned kOddExpLimit = 254u;
+
+__device__ __forceinline__ float partial_as_f32(double x, unsigned& odd_low, unsigned& odd_exp)
+{
+    const unsigned h = (unsigned)__double2hiint(x);
+    const unsigned l = (unsigned)__double2loint(x);
+    odd_low |= l & (h != 0u ? 0x1fffffffu : 0xffffffffu);
+    // biased double exponent 897..1150 <=> fp32 exponent field 1..254 (a set
+    // sign bit lands far above the limit)
+    odd_exp = max(odd_exp, h != 0u ? (h >> 20) - 897u : 0u);
+    // (h:l) << 3 keeps the fp32 exponent field plus 896, modulo 2^9, above
+    // the 23 mantissa bits; adding 2^30 subtracts 896 << 23 modulo 2^32
+    return __uint_as_float(h != 0u ? __funnelshift_l(l, h, 3) + 0x40000000u : 0u);
+}
+
+// One step of Sum2 (Ogita, Rump and Oishi, "Accurate sum and dot product",
+// SIAM J. Sci. Comput. 26(6), 2005): s += p, and the rounding error of that
+// addition, which TwoSum (Knuth) computes exactly, added into c.  After a
+// chain of n non-negative terms with exact sum S, s + c (added in fp64)
+// differs from S by at most gamma(n-1)^2 * S, gamma(k) = k u / (1 - k u) with
+// u = 2^-24, unless s overflowed.  Needs IEEE fp32 addition, round to
+// nearest, subnormals kept (the library is built with -ftz=false).
+__device__ __forceinline__ void sum2_add(float& s, float& c, float p)
+{
+    const float t = s + p;
+    const float z = t - s;
+    c += (s - (t - z)) + (p - z);
+    s = t;
+}
+
 // Sum of the n segment partials in a fixed order, independent of the device:
 // block b of F adds the contiguous range [b*L, (b+1)*L) (L = ceil(n/F)) into
 // stage1[b]; the last block to arrive (an arrival counter, not an ordering)
 // adds stage1[0..F-1] and writes sumsq, the norm, the status word and
-// *norm_out.  No block waits for another.  Each thread adds its terms i,
-// i + 512, ... strictly in that order; the loads of eight consecutive terms
-// are issued before their adds, which leaves the order of the adds (and the
-// bits) as they were.  A partial that is a skipped tile's marker makes the
-// norm NaN and sets the status bits the marker stands for.  On the 1.5B arena
-// (6.1 M partials) the kernel takes 26 us; in a probe a copy that only read
-// the partials took 19 of the 25 us its full form took, the fp64 adds on
-// GB300's narrow FP64 pipe most of the rest.
+// *norm_out.  No block waits for another.
+//
+// Each thread adds its terms i, i + 512, ... in that order by Sum2 in fp32,
+// then the block adds its threads' s + c in fp64 in a fixed tree.  A chain
+// with a partial of another form, or whose fp32 sum overflows, is added
+// again in plain fp64 in the same order (inf and NaN propagate as in any
+// sum, and a skipped tile's marker makes the norm NaN and sets the status
+// bits it stands for).  So the first stage needs no FP64 arithmetic in the
+// usual case: on the 1.5B arena's 6.1 M partials the plain fp64 form took
+// 21.7 us (ncu, cold L2), bound by GB300's FP64 pipe, and this one 13.8 us,
+// bound by load latency.  Chains of one term (n <= 512 F) give the bits the
+// plain fp64 sum gives.
 //
 // The kernel is launched early (programmatic dependent launch): its blocks
 // are placed while the kernel that writes the partials retires, and wait for
@@ -313,23 +355,37 @@ k_norm_finalize(WsHeader* __restrict__ hdr, double* __restrict__ stage1,
     const int64_t lo = (int64_t)blockIdx.x * L;
     const int64_t hi = lo + L < n ? lo + L : n;
     const int64_t bd = blockDim.x;
-    double v = 0.0;
-    unsigned bits = 0;
+    float s = 0.0f, c = 0.0f;
+    unsigned odd_low = 0u, odd_exp = 0u;
     int64_t i = lo + threadIdx.x;
     for (; i + 7 * bd < hi; i += 8 * bd) {
         double x[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) x[k] = __ldcg(&partials[i + k * bd]);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            v += x[k];
-            bits |= marker_bits(x[k]);
-        }
+        for (int k = 0; k < 8; ++k) sum2_add(s, c, partial_as_f32(x[k], odd_low, odd_exp));
     }
-    for (; i < hi; i += bd) {
-        const double x = __ldcg(&partials[i]);
-        v += x;
-        bits |= marker_bits(x);
+    if (i < hi) {      // the last terms, loaded together (indices clamped to the range)
+        double x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int64_t j = i + k * bd;
+            x[k] = __ldcg(&partials[j < hi ? j : hi - 1]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (i + k * bd < hi) sum2_add(s, c, partial_as_f32(x[k], odd_low, odd_exp));
+    }
+    double v = 0.0;
+    unsigned bits = 0;
+    if (odd_low == 0u && odd_exp < kOddExpLimit && isfinite(s)) {
+        v = (double)s + (double)c;
+    } else {
+        for (int64_t q = lo + threadIdx.x; q < hi; q += bd) {
+            const double x = __ldcg(&partials[q]);
+            v += x;
+            bits |= marker_bits(x);
+        }
     }
     v = block_sum(v);
     bits = block_or_bits(bits);

@@ -176,8 +176,9 @@ DPZ_API int dp_allreduce_avg(void* grads, int64_t P, int N, int gdtype,
  * slab c, as left by dp_reduce_scatter_avg): each rank's sum of squares of its
  * shard, then the sum over ranks ("Distributed training", Gates: ZeRO stages
  * differ from DDP only in the order the global norm is summed).  Squares are
- * summed in fp32 within each 256-element segment (a fixed pairwise tree) and
- * in fp64 over segments, in an order fixed by P and N alone, so every entry
+ * summed in fp32 within each 256-element segment (a fixed pairwise tree); the
+ * segment sums are then added in a fixed two-level order (compensated fp32
+ * chains, fp64 beyond them), which depends on P and N alone, so every entry
  * point and every launch configuration gives the same bits.
  * Writes the norm into ws (for zero1_adamw_step) and, if norm_out is not
  * NULL, to *norm_out (device pointer to one float). */
