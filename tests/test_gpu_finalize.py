@@ -51,6 +51,65 @@ def _owner_sumsq(G, N, P):
     return tot
 
 
+def _tree32(x):
+    """The fixed shuffle tree of one warp (offsets 16, 8, 4, 2, 1; lane 0's
+    result) over 32 doubles."""
+    x = x.copy()
+    for o in (16, 8, 4, 2, 1):
+        x[:o] = x[:o] + x[o:2 * o]
+    return x[0]
+
+
+def _block_sum(v):
+    """The block-wide sum of one double per thread (512 threads): each warp's
+    tree, then warp 0's tree over the 16 warp sums (+0 in the other lanes)."""
+    w = np.array([_tree32(v[32 * k:32 * k + 32]) for k in range(len(v) // 32)])
+    return _tree32(np.concatenate([w, np.zeros(32 - len(w))]))
+
+
+def _emulated_sumsq(parts):
+    """The finalisation's documented arithmetic, step by step on the host:
+    F blocks of 512 threads over contiguous ranges, each thread's chain of
+    terms i, i + 512, ... added by Sum2 in fp32 (a TwoSum per term, its error
+    added into c; s + c then in fp64), or in plain fp64 when a term is not +0
+    or a normal fp32 value or the fp32 sum overflows; the block tree; then the
+    sum of the F block sums.  Returns the sum of squares it writes."""
+    n = len(parts)
+    F = min(256, max(1, (n + 2047) // 2048))
+    L = (n + F - 1) // F
+    bits = parts.view(np.uint64)
+    h, l = (bits >> np.uint64(32)).astype(np.uint32), (bits & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    exp = h >> np.uint32(20)
+    normal = (exp >= 897) & (exp <= 1150) & ((l & np.uint32(0x1FFFFFFF)) == 0)
+    ok_term = normal | ((h == 0) & (l == 0))
+    f32 = parts.astype(np.float32)              # exact for the terms that take this path
+    stage1 = np.zeros(F)
+    with np.errstate(over="ignore", invalid="ignore"):
+        for b in range(F):
+            lo, hi = b * L, min(b * L + L, n)
+            v = np.zeros(512)
+            for t in range(512):
+                idx = np.arange(lo + t, hi, 512)
+                if len(idx) and ok_term[idx].all():
+                    s, c = np.float32(0), np.float32(0)
+                    for p in f32[idx]:
+                        tt = np.float32(s + p)
+                        z = np.float32(tt - s)
+                        c = np.float32(c + np.float32(np.float32(s - np.float32(tt - z)) + np.float32(p - z)))
+                        s = tt
+                    if np.isfinite(s):
+                        v[t] = np.float64(s) + np.float64(c)
+                        continue
+                acc = 0.0
+                for p in parts[idx]:
+                    acc = acc + p
+                v[t] = acc
+            stage1[b] = _block_sum(v)
+    w = np.zeros(512)
+    w[:F] = 0.0 + stage1
+    return _block_sum(w)
+
+
 def _norm(G, N, P):
     dpz = _dpz()
     ws = dpz.workspace(P, N, DEV)
@@ -88,6 +147,8 @@ def test_finalize_equals_exact_sum_of_its_partials(N, C, gdt):
     # Sum2 per chain of k terms: within gamma(k-1)^2 of the chain's sum; the
     # fp64 tree and second stage add a few units of 2^-53
     assert abs(got - exact) <= 1e-12 * exact, (got, exact)
+    if n <= 20_000:        # the documented order, bit for bit (host emulation)
+        assert np.float64(got).tobytes() == np.float64(_emulated_sumsq(parts)).tobytes()
     # against the fp64 sum of squares of the values themselves: the segments'
     # fp32 trees are the only other rounding (bound 8 * 2^-24 relative)
     ref = _owner_sumsq(G, N, P)
@@ -105,19 +166,20 @@ def _mid_arena(seed=5):
 
 
 def test_overflowing_chain_is_added_in_fp64():
-    """Owner values of 1e18: every segment's fp32 sum of squares (2.6e38) is
-    finite, the fp32 sum of two of them is not; the chain is added again in
-    fp64 and the norm is finite and correct."""
+    """Owner values in [0.9e18, 1e18]: every segment's fp32 sum of squares
+    (2.1e38 to 2.6e38) is finite, the fp32 sum of two of them is not; every
+    chain is added again in fp64 and the norm is finite and correct."""
     N, C, P, G = _mid_arena()
     g = G.view(N, P)
     for c in range(N):
-        g[c, c * C:(c + 1) * C].uniform_(-1e18, 1e18)
+        g[c, c * C:(c + 1) * C].uniform_(0.9e18, 1e18)
     ws, norm, n = _norm(G, N, P)
     parts = _partials(ws, n)
     assert np.all(np.isfinite(parts)) and parts.max() > 1e38
     exact = math.fsum(parts.tolist())
     assert exact > 3.5e38                              # beyond fp32
     assert abs(_sumsq(ws) - exact) <= 1e-12 * exact
+    assert np.float64(_sumsq(ws)).tobytes() == np.float64(_emulated_sumsq(parts)).tobytes()
     ref = math.sqrt(_owner_sumsq(G, N, P))
     assert math.isfinite(norm) and abs(norm - ref) <= 1e-6 * ref, (norm, ref)
     assert _dpz().ws_status(ws) == 0
@@ -136,6 +198,7 @@ def test_subnormal_partials_are_added_in_fp64():
     assert np.all(tiny < np.float32(1.1754944e-38)) and np.any(tiny > 0)   # subnormal in fp32
     exact = math.fsum(parts.tolist())
     assert abs(_sumsq(ws) - exact) <= 1e-12 * exact
+    assert np.float64(_sumsq(ws)).tobytes() == np.float64(_emulated_sumsq(parts)).tobytes()
     ref = math.sqrt(_owner_sumsq(G, N, P))
     assert abs(norm - ref) <= 1e-6 * ref
     assert _dpz().ws_status(ws) == 0
