@@ -122,3 +122,19 @@ def test_kernel_traffic_follows_its_own_sources(tmp_path, monkeypatch):
         table = json.load(f)
     assert set(table["kernels"]) == set(bench.KERNEL_UNITS)
     assert all(len(k["source_hash"]) == 16 for k in table["kernels"].values())
+
+
+def test_clock_record_rejection_rule():
+    """A slowdown or a clock stuck well below its maximum with no reason makes
+    the timed region invalid (bench.py then takes it again once); the power
+    cap alone does not."""
+    import bench
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 9}
+    assert not bench.clocks_rejected(None)
+    assert not bench.clocks_rejected(full)
+    assert not bench.clocks_rejected(dict(full, sm_mhz=1900.0, reasons=["sw_power_cap"]))
+    assert not bench.clocks_rejected(dict(full, sm_mhz=1500.0, reasons=["sw_power_cap"]))
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.clocks_rejected(dict(full, reasons=[r]))
+    assert bench.clocks_rejected(dict(full, sm_mhz=1200.0))          # a leftover clock lock
+    assert not bench.clocks_rejected(dict(full, sm_mhz=1950.0))
