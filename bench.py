@@ -689,6 +689,25 @@ def time_median(fn, stream, steps: int) -> float:
     return statistics.median(ev[g].elapsed_time(ev[g + 1]) / n for g, n in enumerate(sizes))
 
 
+def warm_up(fn, stream, calls: int, min_ms: float = 20.0) -> None:
+    """`calls` calls of fn, then more until about min_ms of device time has
+    passed in all: right after a large buffer is freed, a new one can run
+    below speed for a few milliseconds (measured: an all-reduce of 2 x 256 MiB
+    took 188 us per call over its first 20 calls after a 56 GB buffer was
+    freed, against 157 us fresh)."""
+    import torch
+    for _ in range(calls):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    one = max(e0.elapsed_time(e1), 1e-3)
+    for _ in range(min(int(min_ms / one), 10000)):
+        fn()
+
+
 def measure_configs(args, dev, stream) -> dict:
     """The other workloads, timed on the device as the headline is (median
     over groups of steps, after warm-up, inputs resident), each in its own
@@ -717,8 +736,7 @@ def measure_configs(args, dev, stream) -> dict:
 
         def step(on=stream):
             dpz.dp_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm, stream=on)
-        for _ in range(max(3, args.warmup)):
-            step()
+        warm_up(step, stream, max(3, args.warmup))
         ms = time_median(step, stream, steps)
         extra = {"clip": w.clip, "steps": steps}
         if w.P * w.N < 1 << 20:
@@ -741,8 +759,7 @@ def measure_configs(args, dev, stream) -> dict:
 
     def allreduce(w, steps):
         G, *_ = allocate(w, dev)
-        for _ in range(max(3, args.warmup)):
-            dpz.dp_allreduce_avg(G, w.N, stream)
+        warm_up(lambda: dpz.dp_allreduce_avg(G, w.N, stream), stream, max(3, args.warmup))
         ms = time_median(lambda: dpz.dp_allreduce_avg(G, w.N, stream), stream, steps)
         del G
         torch.cuda.empty_cache()
