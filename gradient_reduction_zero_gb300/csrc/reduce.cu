@@ -337,10 +337,10 @@ __device__ __forceinline__ void sum2_add(float& s, float& c, float p)
 // again in plain fp64 in the same order (inf and NaN propagate as in any
 // sum, and a skipped tile's marker makes the norm NaN and sets the status
 // bits it stands for).  So the first stage needs no FP64 arithmetic in the
-// usual case: on the 1.5B arena's 6.1 M partials the plain fp64 form took
-// 21.7 us (ncu, cold L2), bound by GB300's FP64 pipe, and this one 13.8 us,
-// bound by load latency.  Chains of one term (n <= 512 F) give the bits the
-// plain fp64 sum gives.
+// usual case: on the 1.5B arena's 6.1 M partials the kernel took 23 us per
+// launch with fp64 chains, bound by GB300's FP64 pipe, and takes 16 us with
+// these, bound by load latency (ncu launch list of the clipped step).  Chains
+// of one term (n <= 512 F) give the bits the plain fp64 sum gives.
 //
 // The kernel is launched early (programmatic dependent launch): its blocks
 // are placed while the kernel that writes the partials retires, and wait for
