@@ -5,6 +5,7 @@
 // ring fold).  AdamW + all-gather from stored averages (the clipped step,
 // dp_zero1_update, dp_zero2_update) is the bulk-copy staged kernel of
 // staged.cu, to which launch_adamw hands that case.
+#include "bulk.cuh"
 #include "device.cuh"
 #include "internal.h"
 
@@ -99,6 +100,7 @@ k_adamw(char* __restrict__ grads, float* __restrict__ master, float* __restrict_
     const int N = NT > 0 ? NT : n_rt;
     const int64_t segs = segments_per_chunk(C);
     const int lane = threadIdx.x & 31;
+    pdl_enter();
     if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     const int64_t sw = global_warp();
     if (sw >= (int64_t)N * segs) return;                 // whole warps
@@ -297,6 +299,7 @@ k_zero1_small(char* __restrict__ grads, float* __restrict__ master, float* __res
     const int team = tid / kTeam, tt = tid % kTeam;
     const int grp = tt >> 2, quarter = tt & 3;       // group of the segment, pair of the group
     const int64_t sw = (int64_t)blockIdx.x * (blockDim.x / kTeam) + team;
+    pdl_enter();
     cluster_arrive_relaxed();      // CTA 0 has started before anyone writes its shared memory
     float s = 0.0f;
     if (sw < total) {                               // whole teams
@@ -341,11 +344,11 @@ static cudaError_t adamw_t(const Arena& a, const Avg& avg, const AdamArgs& h, bo
     const unsigned blocks = blocks_for_segments(int64_t(a.N) * segments_per_chunk(a.C), 1);
     set_last_kernel_name(FOLD ? (SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused")
                               : (BCAST ? "dpz_adamw_bcast" : "dpz_adamw_owner"));
-    k_adamw<GDT, WDT, NT, FOLD, BCAST, SUMSQ><<<blocks, kBlock, 0, s>>>(
-        static_cast<char*>(grads), master, m, v, static_cast<char*>(weights), a.P, a.C, a.N, avg,
-        h, store_avg ? 1 : 0, static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr,
-        avg_stride);
-    return cudaGetLastError();
+    return launch_kernel(k_adamw<GDT, WDT, NT, FOLD, BCAST, SUMSQ>, dim3(blocks), dim3(kBlock), 0, s,
+                         true, 0u, static_cast<char*>(grads), master, m, v,
+                         static_cast<char*>(weights), a.P, a.C, a.N, avg, h, store_avg ? 1 : 0,
+                         static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr,
+                         avg_stride);
 }
 
 // The fold kernel for the arenas the staged kernel does not take (large N
@@ -395,7 +398,7 @@ static cudaError_t small_t(const Arena& a, const Avg& avg, const AdamArgs& h, bo
     const int64_t total = int64_t(a.N) * segments_per_chunk(a.C);
     const unsigned teams = (unsigned)((total + kClusterCtas - 1) / kClusterCtas);   // per CTA
     const unsigned ctas = (unsigned)((total + teams - 1) / teams);                  // <= 8
-    return launch_kernel(k_zero1_small<GDT, WDT, NT>, dim3(ctas), dim3(kTeam * teams), 0, s, false,
+    return launch_kernel(k_zero1_small<GDT, WDT, NT>, dim3(ctas), dim3(kTeam * teams), 0, s, true,
                          ctas, static_cast<char*>(grads), master, m, v,
                          static_cast<char*>(weights), a.P, a.C, a.N, avg, h, store_avg ? 1 : 0,
                          static_cast<WsHeader*>(ws), ws_partials(ws), norm_out);

@@ -69,13 +69,34 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, long long limit
 }
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
-// serialisation may begin once the blocks of the kernel before it on the
-// stream have exited, before that kernel's writes are flushed; wait_prior
-// blocks until every earlier kernel has completed and its writes are visible.
-// In a kernel launched the ordinary way it returns at once.
+// serialisation may begin once every block of the kernel before it on the
+// stream has exited or called pdl_launch_dependents, before that kernel's
+// writes are flushed; wait_prior blocks until every earlier kernel has
+// completed and its writes are visible.  In a kernel launched the ordinary way
+// it returns at once.
 __device__ __forceinline__ void pdl_wait_prior()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel on the stream, if it was launched with programmatic
+// stream serialisation, be placed on the GPU now (it waits for this one with
+// pdl_wait_prior before it touches memory).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// The start of every kernel of this library: wait until the kernels before it
+// on the stream have completed and their writes are visible, then let the
+// next one be placed.  Nothing before this touches global memory, so a call
+// launched early (programmatic stream serialisation) reads what the calls
+// before it wrote, and back-to-back calls overlap one launch with the
+// previous kernel's execution.
+__device__ __forceinline__ void pdl_enter()
+{
+    pdl_wait_prior();
+    pdl_launch_dependents();
 }
 
 // global -> shared, completing `bytes` on the mbarrier

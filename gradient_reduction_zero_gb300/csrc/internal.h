@@ -113,9 +113,10 @@ struct RangeArgs {
 };
 cudaError_t launch_reduce_range(const Arena& a, const Avg& avg, const RangeArgs& g, void* ws,
                                 cudaStream_t s);
-// The finalisation is launched with programmatic stream serialisation: its
-// blocks are placed while the kernel before it retires, and wait for that
-// kernel's writes before they read any partial.
+// Every launcher uses programmatic stream serialisation (launch_kernel with
+// early = true) and every kernel begins with pdl_enter (bulk.cuh): its blocks
+// may be placed while the kernel before it on the stream still runs, and wait
+// for that kernel's writes before they touch memory.
 cudaError_t launch_norm_finalize(const Arena& a, void* ws, float* norm_out, cudaStream_t s);
 // norm_out: where the step's norm went (the bulk-copy staged update writes
 // NaN there if it gives up on a tile; may be NULL).

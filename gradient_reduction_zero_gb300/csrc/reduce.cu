@@ -148,6 +148,7 @@ k_reduce(char* __restrict__ grads, int64_t P, int64_t C, int n_rt, Avg avg,
     const int64_t groups = C / kGroup;
     const int64_t segs = segments_per_chunk(C);
     const int lane = threadIdx.x & 31;
+    pdl_enter();
     if (SUMSQ && blockIdx.x == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     if constexpr (ReduceSegsPerWarp<GDT, NT, ALL>::value > 1) {
         reduce_segments<GDT, NT, ALL, SUMSQ, ReduceSegsPerWarp<GDT, NT, ALL>::value>(
@@ -220,6 +221,7 @@ k_reduce_range(const char* __restrict__ src, int64_t src_stride, char* __restric
     const int64_t segs = segments_per_chunk(C);
     const int lane = threadIdx.x & 31;
     const int64_t sslab = src_stride * ES;
+    pdl_enter();
     if (SUMSQ && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) hdr->arrive = 0u;
     const int c = c_first + (int)blockIdx.y;
     const int64_t plo = lo > c * C ? lo : c * C;
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(kFinalThreads)
 k_norm_finalize(WsHeader* __restrict__ hdr, double* __restrict__ stage1,
                 const double* __restrict__ partials, int64_t n, float* __restrict__ norm_out)
 {
-    pdl_wait_prior();
+    pdl_enter();
     const int F = gridDim.x;
     const int64_t L = (n + F - 1) / F;
     const int64_t lo = (int64_t)blockIdx.x * L;
@@ -438,6 +440,7 @@ k_allgather(char* __restrict__ w, int64_t P, int64_t C, int N)
     const int64_t total = (int64_t)N * segs;
     const int lane = threadIdx.x & 31;
     const int64_t sw0 = global_warp() * U;
+    pdl_enter();
     if (sw0 >= total) return;                             // whole warps
     const SegPos p0 = seg_pos(sw0, segs);
     typename Group<WDT>::Raw x[U];
@@ -470,10 +473,9 @@ static cudaError_t reduce_t(const Arena& a, const Avg& avg, void* grads, void* w
     const unsigned blocks = blocks_for_segments(int64_t(a.N) * segments_per_chunk(a.C),
                                                 ReduceSegsPerWarp<GDT, NT, ALL>::value);
     set_last_kernel_name(ALL ? "dpz_allreduce_avg" : SUMSQ ? "dpz_rs_avg_sumsq" : "dpz_rs_avg");
-    k_reduce<GDT, NT, ALL, SUMSQ><<<blocks, kBlock, 0, s>>>(
-        static_cast<char*>(grads), a.P, a.C, a.N, avg, static_cast<WsHeader*>(ws),
-        SUMSQ ? ws_partials(ws) : nullptr);
-    return cudaGetLastError();
+    return launch_kernel(k_reduce<GDT, NT, ALL, SUMSQ>, dim3(blocks), dim3(kBlock), 0, s, true, 0u,
+                         static_cast<char*>(grads), a.P, a.C, a.N, avg, static_cast<WsHeader*>(ws),
+                         SUMSQ ? ws_partials(ws) : nullptr);
 }
 
 template <int GDT, bool ALL, bool SUMSQ>
@@ -525,11 +527,10 @@ static cudaError_t range_t(const Arena& a, const Avg& avg, const RangeArgs& g, v
         if (grid.x > per_piece) grid.x = per_piece;
     }
     set_last_kernel_name(SUMSQ ? "dpz_rs_range_sumsq" : "dpz_rs_range");
-    k_reduce_range<GDT, NT, SUMSQ><<<grid, kBlock, 0, s>>>(
-        static_cast<const char*>(g.src), g.src_stride, static_cast<char*>(g.dst), g.dst_stride,
-        g.lo, g.hi, a.C, a.N, c_first, avg, static_cast<WsHeader*>(ws),
-        SUMSQ ? ws_partials(ws) : nullptr);
-    return cudaGetLastError();
+    return launch_kernel(k_reduce_range<GDT, NT, SUMSQ>, grid, dim3(kBlock), 0, s, true, 0u,
+                         static_cast<const char*>(g.src), g.src_stride, static_cast<char*>(g.dst),
+                         g.dst_stride, g.lo, g.hi, a.C, a.N, c_first, avg,
+                         static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr);
 }
 
 template <int GDT, bool SUMSQ>
@@ -579,12 +580,10 @@ cudaError_t launch_allgather(const Arena& a, void* weights, cudaStream_t s)
     char* w = static_cast<char*>(weights);
     const int64_t nseg = int64_t(a.N) * segments_per_chunk(a.C);
     if (a.wdt == 1)
-        k_allgather<1><<<blocks_for_segments(nseg, StreamSegs<1>::value), kBlock, 0, s>>>(
-            w, a.P, a.C, a.N);
-    else
-        k_allgather<0><<<blocks_for_segments(nseg, StreamSegs<0>::value), kBlock, 0, s>>>(
-            w, a.P, a.C, a.N);
-    return cudaGetLastError();
+        return launch_kernel(k_allgather<1>, dim3(blocks_for_segments(nseg, StreamSegs<1>::value)),
+                             dim3(kBlock), 0, s, true, 0u, w, a.P, a.C, a.N);
+    return launch_kernel(k_allgather<0>, dim3(blocks_for_segments(nseg, StreamSegs<0>::value)),
+                         dim3(kBlock), 0, s, true, 0u, w, a.P, a.C, a.N);
 }
 
 // ---------------------------------------------------------------------------

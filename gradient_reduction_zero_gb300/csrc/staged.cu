@@ -90,6 +90,7 @@ k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __r
     const int n = (int)(left < kTmaTile ? left : kTmaTile);   // a multiple of 8
     const int tid = threadIdx.x;
 
+    pdl_enter();
     if (tid == 0) {
         mbar_init_one(&full);
         timed_out = 0;
@@ -221,6 +222,7 @@ k_zero1_fused_tma(char* __restrict__ grads, float* __restrict__ master, float* _
     const int tid = threadIdx.x, lane = tid & 31;
     const int64_t gslab = P * GES;
 
+    pdl_enter();
     if (SUMSQ && blockIdx.x == 0 && tid == 0) hdr->arrive = 0u;
     if (tid == 0) {
         mbar_init_one(&full);
@@ -356,6 +358,7 @@ k_norm_owned_tma(const char* __restrict__ grads, int64_t P, int64_t C,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     double* const tile_parts = partials + c * segments_per_chunk(C) + tc * (T / kSegment);
 
+    pdl_enter();
     if (blockIdx.x == 0 && tid == 0) hdr->arrive = 0u;
     if (tid == 0) {
         mbar_init_one(&full);
@@ -435,11 +438,10 @@ cudaError_t tma_t(const Arena& a, const AdamArgs& h, const UpdateLaunch& u, cuda
     if (e != cudaSuccess) return e;
     const int64_t tiles = (a.C + kTmaTile - 1) / kTmaTile * a.N;
     set_last_kernel_name("dpz_adamw_bcast");
-    fn<<<(unsigned)tiles, kTmaThreads, smem, s>>>(
-        static_cast<const char*>(u.grads), u.avg_stride, u.master, u.m, u.v,
-        static_cast<char*>(u.weights), a.P, a.C, a.N, h, static_cast<WsHeader*>(u.ws), u.norm_out,
-        kWaitNormal);
-    return cudaGetLastError();
+    return launch_kernel(fn, dim3((unsigned)tiles), dim3(kTmaThreads), smem, s, true, 0u,
+                         static_cast<const char*>(u.grads), u.avg_stride, u.master, u.m, u.v,
+                         static_cast<char*>(u.weights), a.P, a.C, a.N, h,
+                         static_cast<WsHeader*>(u.ws), u.norm_out, kWaitNormal);
 }
 
 template <int GDT, int WDT>
@@ -526,11 +528,10 @@ static cudaError_t fused_tma_t(const Arena& a, const Avg& avg, const AdamArgs& h
     if (e != cudaSuccess) return e;
     const int64_t tiles = (a.C + TILE - 1) / TILE * a.N;
     set_last_kernel_name(SUMSQ ? "dpz_zero1_fused_sumsq" : "dpz_zero1_fused");
-    fn<<<(unsigned)tiles, TILE / kGroup, smem, s>>>(
-        static_cast<char*>(grads), master, m, v, static_cast<char*>(weights), a.P, a.C, a.N, avg,
-        h, store_avg ? 1 : 0, static_cast<WsHeader*>(ws), SUMSQ ? ws_partials(ws) : nullptr,
-        kWaitNormal);
-    return cudaGetLastError();
+    return launch_kernel(fn, dim3((unsigned)tiles), dim3(TILE / kGroup), smem, s, true, 0u,
+                         static_cast<char*>(grads), master, m, v, static_cast<char*>(weights), a.P,
+                         a.C, a.N, avg, h, store_avg ? 1 : 0, static_cast<WsHeader*>(ws),
+                         SUMSQ ? ws_partials(ws) : nullptr, kWaitNormal);
 }
 
 template <int GDT, int WDT, bool SUMSQ>
@@ -609,10 +610,9 @@ static cudaError_t norm_t(const Arena& a, const void* grads, void* ws, cudaStrea
     auto fn = k_norm_owned_tma<GDT>;
     constexpr size_t smem = (size_t)kNormTile * Group<GDT>::kBytes;   // at most 48 KB
     const int64_t tiles = (a.C + kNormTile - 1) / kNormTile * a.N;
-    fn<<<(unsigned)tiles, kNormThreads, smem, s>>>(
-        static_cast<const char*>(grads), a.P, a.C, static_cast<WsHeader*>(ws), ws_partials(ws),
-        kWaitNormal);
-    return cudaGetLastError();
+    return launch_kernel(fn, dim3((unsigned)tiles), dim3(kNormThreads), smem, s, true, 0u,
+                         static_cast<const char*>(grads), a.P, a.C, static_cast<WsHeader*>(ws),
+                         ws_partials(ws), kWaitNormal);
 }
 
 cudaError_t launch_norm_owned(const Arena& a, const void* grads, void* ws, cudaStream_t s)
