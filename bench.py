@@ -740,7 +740,14 @@ def measure_configs(args, dev, stream) -> dict:
         ms = time_median(step, stream, steps)
         extra = {"clip": w.clip, "steps": steps}
         if w.P * w.N < 1 << 20:
-            # launch-bound: the device time per step with 20 steps in one graph
+            # launch-bound: the same steps through a prepared call (arguments
+            # marshalled once), and the device time per step with 20 steps in
+            # one graph
+            call = dpz.prepare_zero1_step(G, T, M, V, W, w.N, cfg, ws=ws, norm_out=nrm,
+                                          stream=stream)
+            pms = time_median(call, stream, steps)
+            extra.update(prepared_ms_per_step=round(pms, 5),
+                         prepared_steps_per_s=round(1e3 / pms, 1))
             side = torch.cuda.Stream()
             side.wait_stream(stream)
             g = torch.cuda.CUDAGraph()
@@ -761,9 +768,15 @@ def measure_configs(args, dev, stream) -> dict:
         G, *_ = allocate(w, dev)
         warm_up(lambda: dpz.dp_allreduce_avg(G, w.N, stream), stream, max(3, args.warmup))
         ms = time_median(lambda: dpz.dp_allreduce_avg(G, w.N, stream), stream, steps)
+        extra = {"steps": steps}
+        if w.P * w.N < 1 << 20:
+            call = dpz.prepare_allreduce_avg(G, w.N, stream=stream)
+            pms = time_median(call, stream, steps)
+            extra.update(prepared_ms_per_step=round(pms, 5),
+                         prepared_steps_per_s=round(1e3 / pms, 1))
         del G
         torch.cuda.empty_cache()
-        return row(w, ms, {"steps": steps})
+        return row(w, ms, extra)
 
     rows[I.TINY.name] = zero1(I.TINY, 2000)
     rows[I.GPT2_124M.name] = zero1(I.GPT2_124M, 50)
