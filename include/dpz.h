@@ -49,7 +49,12 @@
  *
  * Streams: the caller orders producers of `grads` before the call with
  * events (A4 Part 3: record an event on the compute stream, make the
- * communication stream wait on it), and consumers after it.
+ * communication stream wait on it), and consumers after it.  Every kernel is
+ * launched with programmatic stream serialisation: its blocks may be placed
+ * while the kernel before it on the same stream still runs, and they wait
+ * for that kernel to complete (its writes visible) before they touch memory.
+ * So the calls keep the stream's order after a kernel, a copy or an event
+ * wait alike.
  *
  * CUDA graphs: every compute call except dp_grad_global_norm_static only
  * enqueues kernels on `stream`, so it can be captured into a CUDA graph and
