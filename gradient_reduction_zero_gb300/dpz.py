@@ -114,28 +114,33 @@ def _torch():
     return torch
 
 
+_CODES: dict = {}
+
+
 def dtype_code(t, acc32: bool = False) -> int:
     """DPZ dtype code of a tensor; acc32 selects the fp32-accumulating ring for
     a bf16 gradient arena."""
-    torch = _torch()
-    if t.dtype == torch.bfloat16:
-        return BF16_ACC32 if acc32 else BF16
+    if not _CODES:
+        torch = _torch()
+        _CODES.update({torch.bfloat16: BF16, torch.float32: F32})
+    code = _CODES.get(t.dtype)
+    if code is None:
+        raise TypeError(f"unsupported dtype {t.dtype}")
     if acc32:
-        raise TypeError("fp32 accumulation applies to bf16 gradient arenas")
-    if t.dtype == torch.float32:
-        return F32
-    raise TypeError(f"unsupported dtype {t.dtype}")
+        if code != BF16:
+            raise TypeError("fp32 accumulation applies to bf16 gradient arenas")
+        return BF16_ACC32
+    return code
 
 
 def _stream_handle(stream) -> int:
-    torch = _torch()
     if stream is None:
-        stream = torch.cuda.current_stream()
-    return int(stream.cuda_stream)
+        stream = _torch().cuda.current_stream()
+    return stream.cuda_stream
 
 
 def _ptr(t) -> int | None:
-    return None if t is None else int(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def make_cfg(lr, beta1, beta2, eps, weight_decay, step, clip_norm=0.0, store_avg=False) -> AdamWCfg:
@@ -152,9 +157,10 @@ def workspace(P: int, N: int, device=None):
 
 
 def _np(arena, N: int) -> int:
-    if arena.numel() % N:
+    n = arena.numel()
+    if n % N:
         raise ValueError("arena size is not a multiple of N")
-    return arena.numel() // N
+    return n // N
 
 
 # ------------------------------------------------------------ the calls
