@@ -1,7 +1,10 @@
-"""Build libdpz.so in-tree with nvcc for sm_103a (no cmake, one -gencode).
+"""Build libdpz.so in-tree with nvcc for sm_103a (no cmake, one -gencode),
+then the CPython module _dpzcall that calls it from Python.
 
 Translation units compile in parallel; the shared library links the CUDA
-runtime statically, so loading it needs no GPU.
+runtime statically, so loading it needs no GPU.  _dpzcall (csrc/pycall.c) is
+plain C against Python.h and libdpz.so; where Python's headers are missing
+the binding calls the library through ctypes instead.
 """
 from __future__ import annotations
 
@@ -52,6 +55,41 @@ def _compile(src: str) -> str:
     return obj
 
 
+PYCALL_SRC = os.path.join(CSRC, "pycall.c")
+
+
+def pycall_path() -> str:
+    import sysconfig
+    return os.path.join(PKG, "_dpzcall" + sysconfig.get_config_var("EXT_SUFFIX"))
+
+
+def build_pycall(verbose: bool = False) -> str | None:
+    """Compile _dpzcall (if anything changed); None where Python's headers are
+    not installed."""
+    import sysconfig
+    inc = sysconfig.get_paths()["include"]
+    if not os.path.exists(os.path.join(inc, "Python.h")):
+        if verbose:
+            print(f"no Python.h under {inc}: the binding calls libdpz.so through ctypes",
+                  file=sys.stderr)
+        return None
+    out = pycall_path()
+    if _stale(out, [PYCALL_SRC, os.path.join(INCLUDE, "dpz.h"), LIB]):
+        tmp = out + f".tmp{os.getpid()}"
+        try:
+            subprocess.check_call([os.environ.get("CC", "gcc"), "-O2", "-std=c11", "-shared",
+                                   "-fPIC", "-I" + inc, "-I" + INCLUDE, PYCALL_SRC, "-L" + PKG,
+                                   "-ldpz", "-Wl,-rpath,$ORIGIN", "-o", tmp])
+        except (OSError, subprocess.CalledProcessError) as e:
+            print(f"_dpzcall not built ({e}): the binding calls libdpz.so through ctypes",
+                  file=sys.stderr)
+            return None
+        os.replace(tmp, out)
+    if verbose:
+        print(f"built {out}", file=sys.stderr)
+    return out
+
+
 def build(verbose: bool = False) -> str:
     """Compile (if anything changed) and return the path of libdpz.so."""
     os.makedirs(BUILD, exist_ok=True)
@@ -64,6 +102,7 @@ def build(verbose: bool = False) -> str:
         os.replace(tmp, LIB)
     if verbose:
         print(f"built {LIB}", file=sys.stderr)
+    build_pycall(verbose)
     return LIB
 
 

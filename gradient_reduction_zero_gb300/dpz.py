@@ -51,10 +51,10 @@ _SIGS = {
     "dp_grad_global_norm": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _VP, _FP, _VP],
                             ctypes.c_int),
     "zero1_adamw_step": ([_VP, _FP, _FP, _FP, _VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
-                          ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _VP], ctypes.c_int),
+                          ctypes.c_int, _VP, _VP, _VP], ctypes.c_int),
     "dp_allgather": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _VP], ctypes.c_int),
     "dp_zero1_step": ([_VP, _FP, _FP, _FP, _VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
-                       ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _FP, _VP], ctypes.c_int),
+                       ctypes.c_int, _VP, _VP, _FP, _VP], ctypes.c_int),
     "dp_grad_global_norm_static": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _FP, _VP],
                                    ctypes.c_int),
     "dp_reduce_scatter_avg_range": ([_VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
@@ -65,9 +65,9 @@ _SIGS = {
                                      ctypes.c_int),
     "dp_grad_norm_finalize": ([_VP, ctypes.c_int64, ctypes.c_int, _FP, _VP], ctypes.c_int),
     "dp_zero1_update": ([_VP, _FP, _FP, _FP, _VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
-                         ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _VP], ctypes.c_int),
+                         ctypes.c_int, _VP, _VP, _VP], ctypes.c_int),
     "dp_zero2_update": ([_VP, _FP, _FP, _FP, _VP, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
-                         ctypes.c_int, ctypes.POINTER(AdamWCfg), _VP, _VP], ctypes.c_int),
+                         ctypes.c_int, _VP, _VP, _VP], ctypes.c_int),
     "dpz_last_error": ([], ctypes.c_char_p),
     "dpz_version": ([], ctypes.c_char_p),
     "dpz_launch_count": ([], ctypes.c_int64),
@@ -94,6 +94,20 @@ def _load() -> ctypes.CDLL:
 
 
 lib = _load()
+
+
+def _load_call():
+    """The CPython module that makes the compute calls (loaded after lib, so
+    that both use the one loaded libdpz.so); lib itself where it was not
+    built.  Both take the same arguments: Python ints, None for NULL."""
+    try:
+        from . import _dpzcall
+    except ImportError:
+        return lib
+    return _dpzcall
+
+
+_C = _load_call()
 
 
 def header_symbols(path: str = HEADER) -> list[str]:
@@ -166,43 +180,43 @@ def _np(arena, N: int) -> int:
 # ------------------------------------------------------------ the calls
 
 def dp_reduce_scatter_avg(grads, N: int, stream=None, acc32: bool = False) -> None:
-    _check(lib.dp_reduce_scatter_avg(_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32),
+    _check(_C.dp_reduce_scatter_avg(_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32),
                                      _stream_handle(stream)))
 
 
 def dp_allreduce_avg(grads, N: int, stream=None, acc32: bool = False) -> None:
-    _check(lib.dp_allreduce_avg(_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32),
+    _check(_C.dp_allreduce_avg(_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32),
                                 _stream_handle(stream)))
 
 
 def dp_grad_global_norm(grads, N: int, ws, norm_out=None, stream=None) -> None:
-    _check(lib.dp_grad_global_norm(_ptr(grads), _np(grads, N), N, dtype_code(grads), _ptr(ws),
+    _check(_C.dp_grad_global_norm(_ptr(grads), _np(grads, N), N, dtype_code(grads), _ptr(ws),
                                    _ptr(norm_out), _stream_handle(stream)))
 
 
 def dp_grad_global_norm_static(grads, N: int, norm_out, stream=None) -> None:
     """The global norm without a caller workspace (fixed device scratch)."""
-    _check(lib.dp_grad_global_norm_static(_ptr(grads), _np(grads, N), N, dtype_code(grads),
+    _check(_C.dp_grad_global_norm_static(_ptr(grads), _np(grads, N), N, dtype_code(grads),
                                           _ptr(norm_out), _stream_handle(stream)))
 
 
 def zero1_adamw_step(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None,
                      stream=None) -> None:
-    _check(lib.zero1_adamw_step(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
+    _check(_C.zero1_adamw_step(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
                                 _np(grads, N), N, dtype_code(grads), dtype_code(weights),
-                                ctypes.byref(cfg), _ptr(ws), _stream_handle(stream)))
+                                ctypes.addressof(cfg), _ptr(ws), _stream_handle(stream)))
 
 
 def dp_allgather(weights, N: int, stream=None) -> None:
-    _check(lib.dp_allgather(_ptr(weights), _np(weights, N), N, dtype_code(weights),
+    _check(_C.dp_allgather(_ptr(weights), _np(weights, N), N, dtype_code(weights),
                             _stream_handle(stream)))
 
 
 def dp_zero1_step(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None, norm_out=None,
                   stream=None, acc32: bool = False) -> None:
-    _check(lib.dp_zero1_step(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
+    _check(_C.dp_zero1_step(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
                              _np(grads, N), N, dtype_code(grads, acc32), dtype_code(weights),
-                             ctypes.byref(cfg), _ptr(ws), _ptr(norm_out),
+                             ctypes.addressof(cfg), _ptr(ws), _ptr(norm_out),
                              _stream_handle(stream)))
 
 
@@ -210,7 +224,7 @@ def dp_reduce_scatter_avg_range(grads, N: int, lo: int, n: int, ws=None, stream=
                                 acc32: bool = False, max_ctas: int = 0) -> None:
     """max_ctas: 0 = one pass over the range; > 0 caps the kernel's blocks
     (for example one per SM) to leave the GPU to kernels on other streams."""
-    _check(lib.dp_reduce_scatter_avg_range(_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32),
+    _check(_C.dp_reduce_scatter_avg_range(_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32),
                                            lo, n, _ptr(ws), max_ctas, _stream_handle(stream)))
 
 
@@ -219,27 +233,27 @@ def dp_reduce_scatter_avg_bucket(staging, lo: int, shards, N: int, ws=None, stre
     """staging: [N*n] (rank r's values of arena elements [lo, lo+n) at r*n);
     shards: [P].  max_ctas as in dp_reduce_scatter_avg_range."""
     n = _np(staging, N)
-    _check(lib.dp_reduce_scatter_avg_bucket(_ptr(staging), lo, n, _ptr(shards), shards.numel(),
+    _check(_C.dp_reduce_scatter_avg_bucket(_ptr(staging), lo, n, _ptr(shards), shards.numel(),
                                             N, dtype_code(staging, acc32), _ptr(ws), max_ctas,
                                             _stream_handle(stream)))
 
 
 def dp_grad_norm_finalize(ws, P: int, N: int, norm_out=None, stream=None) -> None:
-    _check(lib.dp_grad_norm_finalize(_ptr(ws), P, N, _ptr(norm_out), _stream_handle(stream)))
+    _check(_C.dp_grad_norm_finalize(_ptr(ws), P, N, _ptr(norm_out), _stream_handle(stream)))
 
 
 def dp_zero1_update(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None,
                     stream=None) -> None:
-    _check(lib.dp_zero1_update(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
+    _check(_C.dp_zero1_update(_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
                                _np(grads, N), N, dtype_code(grads), dtype_code(weights),
-                               ctypes.byref(cfg), _ptr(ws), _stream_handle(stream)))
+                               ctypes.addressof(cfg), _ptr(ws), _stream_handle(stream)))
 
 
 def dp_zero2_update(shards, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None,
                     stream=None) -> None:
-    _check(lib.dp_zero2_update(_ptr(shards), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
+    _check(_C.dp_zero2_update(_ptr(shards), _ptr(master), _ptr(m), _ptr(v), _ptr(weights),
                                shards.numel(), N, dtype_code(shards), dtype_code(weights),
-                               ctypes.byref(cfg), _ptr(ws), _stream_handle(stream)))
+                               ctypes.addressof(cfg), _ptr(ws), _stream_handle(stream)))
 
 
 class PreparedCall:
@@ -262,25 +276,28 @@ class PreparedCall:
             _check(rc)
 
 
-def _void_p(t):
-    return ctypes.c_void_p(_ptr(t))
+def _prepare(name: str, args: tuple, keep) -> PreparedCall:
+    """A PreparedCall of the compute call `name` with `args` (Python ints,
+    None for NULL).  Through ctypes they are converted here, once."""
+    fn = getattr(_C, name)
+    if _C is lib:
+        args = tuple(t(v) for t, v in zip(fn.argtypes, args))
+    return PreparedCall(fn, args, keep)
 
 
 def prepare_zero1_step(grads, master, m, v, weights, N: int, cfg: AdamWCfg, ws=None,
                        norm_out=None, stream=None, acc32: bool = False) -> PreparedCall:
     """dp_zero1_step with its arguments marshalled once (PreparedCall)."""
-    args = (_void_p(grads), _void_p(master), _void_p(m), _void_p(v), _void_p(weights),
-            ctypes.c_int64(_np(grads, N)), ctypes.c_int(N), ctypes.c_int(dtype_code(grads, acc32)),
-            ctypes.c_int(dtype_code(weights)), ctypes.byref(cfg), _void_p(ws), _void_p(norm_out),
-            ctypes.c_void_p(_stream_handle(stream)))
-    return PreparedCall(lib.dp_zero1_step, args, (grads, master, m, v, weights, cfg, ws, norm_out))
+    args = (_ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(weights), _np(grads, N), N,
+            dtype_code(grads, acc32), dtype_code(weights), ctypes.addressof(cfg), _ptr(ws),
+            _ptr(norm_out), _stream_handle(stream))
+    return _prepare("dp_zero1_step", args, (grads, master, m, v, weights, cfg, ws, norm_out))
 
 
 def prepare_allreduce_avg(grads, N: int, stream=None, acc32: bool = False) -> PreparedCall:
     """dp_allreduce_avg with its arguments marshalled once (PreparedCall)."""
-    args = (_void_p(grads), ctypes.c_int64(_np(grads, N)), ctypes.c_int(N),
-            ctypes.c_int(dtype_code(grads, acc32)), ctypes.c_void_p(_stream_handle(stream)))
-    return PreparedCall(lib.dp_allreduce_avg, args, (grads,))
+    args = (_ptr(grads), _np(grads, N), N, dtype_code(grads, acc32), _stream_handle(stream))
+    return _prepare("dp_allreduce_avg", args, (grads,))
 
 
 def launch_count() -> int:

@@ -232,3 +232,34 @@ def test_prepared_call_validates_every_call(dpz):
     ar = dpz.prepare_allreduce_avg(G, N, stream=NoStream())
     with pytest.raises(dpz.DpzError):
         ar()
+
+
+def test_call_module_covers_the_compute_calls(dpz):
+    """The CPython call module (built where Python's headers are installed)
+    exposes every compute call of the header with its arity, takes ints and
+    None, and shares the one loaded libdpz.so with the ctypes binding: its
+    errors read back through dpz_last_error."""
+    if dpz._C is dpz.lib:
+        pytest.skip("_dpzcall was not built here (no Python headers)")
+    calls = {"dp_reduce_scatter_avg": 5, "dp_allreduce_avg": 5, "dp_grad_global_norm": 7,
+             "dp_grad_global_norm_static": 6, "zero1_adamw_step": 12, "dp_allgather": 5,
+             "dp_zero1_step": 13, "dp_reduce_scatter_avg_range": 9,
+             "dp_reduce_scatter_avg_bucket": 10, "dp_grad_norm_finalize": 5,
+             "dp_zero1_update": 12, "dp_zero2_update": 12}
+    declared = set(dpz.header_symbols())
+    for name, arity in calls.items():
+        assert name in declared, name
+        assert len(getattr(dpz.lib, name).argtypes) == arity, name
+        fn = getattr(dpz._C, name)
+        with pytest.raises(TypeError):
+            fn(*([None] * (arity - 1)))
+    # every compute call the header declares is in the module
+    compute = {n for n in declared if n.startswith(("dp_", "zero1_"))}
+    assert compute == set(calls)
+    assert dpz._C.dp_allreduce_avg(None, 4096, 0, dpz.F32, None) == dpz.ERR_INVALID_ARG
+    assert b"N = 0" in dpz.lib.dpz_last_error()
+    assert dpz._C.dp_zero1_step(None, None, None, None, None, 4096, 4, dpz.F32, dpz.BF16,
+                                None, None, None, None) == dpz.ERR_INVALID_ARG
+    assert b"cfg is NULL" in dpz.lib.dpz_last_error()
+    with pytest.raises(OverflowError):
+        dpz._C.dp_allreduce_avg(None, 4096, 1 << 40, dpz.F32, None)
