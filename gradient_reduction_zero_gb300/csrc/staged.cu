@@ -2,7 +2,7 @@
 // (TMA, 1-D cp.async.bulk; bulk.cuh), all three on one-shot, chunk-major grids:
 //
 // - AdamW + cast + all-gather of the new weights from the stored averages:
-//   one 1024-element tile per 128-thread CTA.  Thread 0 issues the bulk loads
+//   one 2048-element tile per 256-thread CTA.  Thread 0 issues the bulk loads
 //   of the tile's averaged gradient and master/m/v, completing on one
 //   mbarrier; every thread updates 8 elements in shared memory; thread 0 then
 //   bulk-stores master/m/v and the cast weights into the N weight slabs and
@@ -34,8 +34,15 @@
 
 namespace dpz {
 
-constexpr int kTmaTile = 1024;                     // elements per CTA
+constexpr int kTmaTile = 1024;                     // elements per CTA of the step without clip
 constexpr int kTmaThreads = kTmaTile / kGroup;     // 128: 8 elements each
+// The AdamW + broadcast kernel's tile: 2048 elements per 256-thread CTA, five
+// CTAs per SM.  Against 1024-element tiles (128 threads, ten per SM), same
+// bits, the clipped steps measured 8-11 us faster at 1.5B and 3 us at 124M
+// on two boxes; 512-element tiles were slower, and 4096-element tiles (two
+// CTAs per SM) much slower.
+constexpr int kUpdateTile = 2048;
+constexpr int kUpdateThreads = kUpdateTile / kGroup;
 
 __device__ unsigned g_pipeline_error;
 
@@ -51,11 +58,11 @@ __device__ __forceinline__ float quiet_nan() { return __int_as_float(0x7fc00000)
 
 template <int GDT, int WDT>
 struct TmaTile {
-    unsigned char avg[kTmaTile * Group<GDT>::kBytes];
-    float th[kTmaTile];
-    float m[kTmaTile];
-    float v[kTmaTile];
-    unsigned char w[kTmaTile * Group<WDT>::kBytes];
+    unsigned char avg[kUpdateTile * Group<GDT>::kBytes];
+    float th[kUpdateTile];
+    float m[kUpdateTile];
+    float v[kUpdateTile];
+    unsigned char w[kUpdateTile * Group<WDT>::kBytes];
 };
 
 // grads: the averaged gradient of element e (chunk c) at grads + (c*avg_stride
@@ -63,9 +70,9 @@ struct TmaTile {
 // status word, where a skipped tile is reported; may be NULL without clip);
 // norm_out: set to NaN if this kernel gives up on a tile (may be NULL).
 // NT > 0: N == NT known at compile time; NT == 0: any N, read from n_rt.
-// Ten CTAs per SM (at most 48 registers a thread).
+// Five CTAs per SM (at most 51 registers a thread).
 template <int GDT, int WDT, int NT>
-__global__ void __launch_bounds__(kTmaThreads, 10)
+__global__ void __launch_bounds__(kUpdateThreads, 5)
 k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __restrict__ master,
                   float* __restrict__ mom, float* __restrict__ var, char* __restrict__ weights,
                   int64_t P, int64_t C, int n_rt, AdamArgs h, WsHeader* __restrict__ hdr,
@@ -82,12 +89,12 @@ k_adamw_bcast_tma(const char* __restrict__ grads, int64_t avg_stride, float* __r
     __shared__ int timed_out;
 
     // tile b of the chunk-major tile list: chunk c, first element e, n elements
-    const int64_t tiles_per_chunk = (C + kTmaTile - 1) / kTmaTile;
+    const int64_t tiles_per_chunk = (C + kUpdateTile - 1) / kUpdateTile;
     const int c = (int)(blockIdx.x / tiles_per_chunk);
     const int64_t tc = blockIdx.x - (int64_t)c * tiles_per_chunk;
-    const int64_t e = (int64_t)c * C + tc * kTmaTile;
-    const int64_t left = C - tc * kTmaTile;
-    const int n = (int)(left < kTmaTile ? left : kTmaTile);   // a multiple of 8
+    const int64_t e = (int64_t)c * C + tc * kUpdateTile;
+    const int64_t left = C - tc * kUpdateTile;
+    const int n = (int)(left < kUpdateTile ? left : kUpdateTile);   // a multiple of 8
     const int tid = threadIdx.x;
 
     pdl_enter();
@@ -436,9 +443,9 @@ cudaError_t tma_t(const Arena& a, const AdamArgs& h, const UpdateLaunch& u, cuda
     const size_t smem = sizeof(TmaTile<GDT, WDT>);
     const cudaError_t e = allow_smem(raised, reinterpret_cast<const void*>(fn), smem);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = (a.C + kTmaTile - 1) / kTmaTile * a.N;
+    const int64_t tiles = (a.C + kUpdateTile - 1) / kUpdateTile * a.N;
     set_last_kernel_name("dpz_adamw_bcast");
-    return launch_kernel(fn, dim3((unsigned)tiles), dim3(kTmaThreads), smem, s, true, 0u,
+    return launch_kernel(fn, dim3((unsigned)tiles), dim3(kUpdateThreads), smem, s, true, 0u,
                          static_cast<const char*>(u.grads), u.avg_stride, u.master, u.m, u.v,
                          static_cast<char*>(u.weights), a.P, a.C, a.N, h,
                          static_cast<WsHeader*>(u.ws), u.norm_out, kWaitNormal);
@@ -665,7 +672,7 @@ cudaError_t launch_staged_timeout_selftest(int kernel, void* buf, cudaStream_t s
         e = allow_smem(raised, reinterpret_cast<const void*>(fn), smem);
         if (e != cudaSuccess) return e;
         set_last_kernel_name("dpz_selftest_staged_timeout");
-        fn<<<1, kTmaThreads, smem, s>>>(grads, a.P, master, m, v, weights, a.P, a.C, 1, h, hdr,
+        fn<<<1, kUpdateThreads, smem, s>>>(grads, a.P, master, m, v, weights, a.P, a.C, 1, h, hdr,
                                        norm_out, wait);
         return cudaGetLastError();
     }
